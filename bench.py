@@ -1,0 +1,404 @@
+#!/usr/bin/env python
+"""Benchmark of the paged sink-attention hot path on GB300.
+
+Headline (`value`): decode attention on the gpt-oss-120b-shaped batch (64
+requests, kv_len ~ U[1024, 8192], Hq 64 / Hkv 8, head_dim 64, 16-token HND
+pages, split-KV), reported as algorithmic KV bytes read per second (GB/s):
+sum over requests of kv_len * Hkv * head_dim * 2 (K and V) * 2 bytes, divided
+by the device time of one attn_decode launch (which includes the split-KV
+merge).  Inputs are resident in HBM; the KV pool (about 750 MB) is larger
+than L2, and L2 is also flushed (a 256 MB memset, outside the timed events)
+before every timed step.  The prefill leg (gpt-oss-120b-shaped ragged causal
+prefill) is reported in TFLOP/s of visible (query, key) pairs x 4 * head_dim.
+
+One step = one pass of the hot path over one batch: the plan is built once
+per batch (host), then attn_decode runs (and attn_prefill for the prefill
+leg).  `e2e` times the same decode through the public API from pinned host
+buffers: H2D of q and the page table, planning and work-list upload, the
+launch, and D2H of out and lse, every step.
+
+Multi-GPU: the path shards by request with no exchange, so N ranks run N
+independent replicas ("scaling": "weak"); value = all ranks' bytes / max
+rank time.  `--impl reference` times the CPU fp64 oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "decode attn KV-read GB/s vs ~8 TB/s HBM; prefill attn TFLOP/s vs bf16 peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kv_bytes(batch, rows_only=None):
+    """Algorithmic KV bytes of the decode requests (K and V of every valid token)."""
+    per_tok = batch.num_kv_heads * batch.head_dim * 2 * 2
+    kv = batch.kv_lens[batch.qo_lens == 1] if rows_only is None else rows_only
+    return int(np.sum(kv)) * per_tok
+
+
+def prefill_flops(batch):
+    pairs = 0
+    for b in range(batch.batch_size):
+        qo, kv = int(batch.qo_lens[b]), int(batch.kv_lens[b])
+        if qo > 1:
+            prefix = kv - qo
+            pairs += qo * prefix + qo * (qo + 1) // 2 if batch.causal else qo * kv
+    return pairs * batch.num_qo_heads * 4 * batch.head_dim
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [l.strip().split(", ") for l in self.file.read().splitlines() if l.strip()]
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[0]))
+                smax.append(float(r[1]))
+                for name, v in zip(names, r[4:8]):
+                    if v.strip().lower() == "active":
+                        reasons.add(name)
+            except (ValueError, IndexError):
+                continue
+        busy = [s for s in sm if smax and s > 0.5 * max(smax)] or sm
+        return {"sm_mhz": statistics.median(busy) if busy else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# -------------------------------------------------------------- distributed
+def dist_setup(impl):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if impl == "ours" else "gloo"
+        if backend == "nccl":
+            import torch
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------- reference arm
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import oracle
+    from paged_kv_attention_sink_gb300 import synthetic as syn
+    oracle.build()
+    batch = syn.gptoss_decode(0)
+    cores = os.cpu_count() or 1
+    # Each step: the oracle over a fixed sample of 8 requests (all 64 heads).
+    rows = np.arange(8, dtype=np.int64)
+    rr = np.repeat(rows, batch.num_qo_heads)
+    hh = np.tile(np.arange(batch.num_qo_heads, dtype=np.int32), len(rows))
+    sample_bytes = kv_bytes(batch, rows_only=batch.kv_lens[:8])
+    for _ in range(args.warmup):
+        oracle.sink_attention(batch, rows=rr, heads=hh, n_threads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.sink_attention(batch, rows=rr, heads=hh, n_threads=cores)
+    dt = time.perf_counter() - t0
+    value = sample_bytes * args.steps / dt / 1e9
+    sample = "gptoss_decode seed 0, requests 0-7 (all 64 query heads), fp64 C oracle per step"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "gptoss_decode", "batch": batch.batch_size, "Hq": 64, "Hkv": 8,
+                   "head_dim": 64, "page_size": 16, "kv_len": "U[1024,8192]"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# ---------------------------------------------------------------- our arm
+def traffic_for(kernel_file, key):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source
+    is unchanged since the capture (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        table = json.load(f)
+    entry = table.get(key)
+    if not entry:
+        return None
+    src = os.path.join(ROOT, "paged_kv_attention_sink_gb300", "csrc", kernel_file)
+    with open(src, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()
+    return entry["dram_bytes_per_launch"] if entry.get("source_sha256") == sha else None
+
+
+def time_device(fn, steps, flush, stream):
+    import torch
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        starts[i].record(stream)
+        fn()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    from paged_kv_attention_sink_gb300 import build as libbuild
+    libbuild.build()
+    from paged_kv_attention_sink_gb300 import binding, synthetic as syn
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    peaks, peak_src = load_peaks()
+
+    def to_dev(batch):
+        q = torch.from_numpy(batch.q.view(np.int16)).view(torch.bfloat16).to(dev)
+        kv = torch.from_numpy(batch.kv_pool.view(np.int16)).view(torch.bfloat16).to(dev)
+        pt = torch.from_numpy(batch.page_table).to(dev)
+        sk = None if batch.sinks is None else torch.from_numpy(batch.sinks).to(dev)
+        return q, kv, pt, sk
+
+    def plan_of(batch, pt):
+        return binding.Plan(batch.qo_indptr, batch.kv_indptr, pt, batch.last_page_len,
+                            batch.num_qo_heads, batch.num_kv_heads, batch.head_dim, batch.page_size,
+                            causal=batch.causal, sm_scale=batch.sm_scale, num_pages=batch.num_pages)
+
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = getattr(props, "uuid", None)
+    gpu_id = ("GPU-" + str(gpu_id)) if gpu_id is not None and not str(gpu_id).startswith("GPU-") else str(gpu_id or local)
+
+    # ---- decode (headline)
+    batch = syn.gptoss_decode(seed=rank)
+    q, kv, pt, sinks = to_dev(batch)
+    t0 = time.perf_counter()
+    plan = plan_of(batch, pt)
+    plan_us = (time.perf_counter() - t0) * 1e6
+    out = torch.empty_like(q)
+    lse = torch.empty(batch.total_rows, batch.num_qo_heads, device=dev)
+    dec = lambda: plan.decode(q, kv, sinks, out, lse)
+    for _ in range(args.warmup):
+        flush.zero_()
+        dec()
+    torch.cuda.synchronize()
+    if plan.device_error():
+        raise RuntimeError("decode kernel recorded a device error")
+
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    times = time_device(dec, args.steps, flush, stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    total_ms = max_over_ranks(sum(times), world)
+    bytes_step = kv_bytes(batch)
+    value = world * bytes_step * args.steps / (total_ms / 1e3) / 1e9
+    mean_s = sum(times) / len(times) / 1e3
+    achieved = bytes_step / mean_s / 1e9
+    peak = float(peaks["hbm_gbs"])
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": traffic_for("decode.cu", "decode_gptoss"),
+                "kernel": "decode_sink_attn_kernel<64,false>", "peak_source": peak_src,
+                "frac_of_nominal_8TBps": achieved / 8000.0}
+
+    # ---- e2e through the public API from pinned host buffers
+    q_h = torch.from_numpy(batch.q.view(np.int16)).view(torch.bfloat16).pin_memory()
+    pt_h = torch.from_numpy(batch.page_table).pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    q_d = torch.empty_like(q)
+    pt_d = torch.empty_like(pt)
+    e2e_steps = max(3, min(args.steps, 200))
+
+    def e2e_step():
+        q_d.copy_(q_h, non_blocking=True)
+        pt_d.copy_(pt_h, non_blocking=True)
+        p = plan_of(batch, pt_d)
+        p.decode(q_d, kv, sinks, out, lse)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+        torch.cuda.synchronize()
+        return p
+
+    for _ in range(3):
+        e2e_step()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    units = plan.info()["num_decode_units"]
+    h2d = q_h.numel() * 2 + pt_h.numel() * 4 + units * 48
+    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+    e2e = {"value": world * bytes_step * e2e_steps / e2e_s / 1e9, "unit": "GB/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "ms_per_step": e2e_s * 1e3 / e2e_steps}
+
+    # ---- prefill leg (TFLOP/s), if the kernel is available
+    prefill = None
+    launches = args.steps
+    if not args.no_prefill:
+        pbatch = syn.gptoss_prefill(seed=rank)
+        pq, pkv, ppt, psk = to_dev(pbatch)
+        pplan = plan_of(pbatch, ppt)
+        pout = torch.empty_like(pq)
+        plse = torch.empty(pbatch.total_rows, pbatch.num_qo_heads, device=dev)
+        pre = lambda: pplan.prefill(pq, pkv, psk, pout, plse)
+        try:
+            pre()
+            torch.cuda.synchronize()
+        except binding.AttnError as e:
+            prefill = {"unavailable": str(e)}
+        if prefill is None:
+            for _ in range(args.warmup):
+                pre()
+            torch.cuda.synchronize()
+            psteps = max(3, args.steps // 10)
+            ptimes = time_device(pre, psteps, flush, stream)
+            pmean = sum(ptimes) / len(ptimes) / 1e3
+            flops = prefill_flops(pbatch)
+            tf = flops / pmean / 1e12
+            ppeak = float(peaks["bf16_tflops"])
+            prefill = {"workload": "gptoss_prefill", "value": tf, "unit": "TFLOP/s",
+                       "ms_per_step": pmean * 1e3, "steps": psteps,
+                       "roofline": {"bound": "tensor", "achieved": tf, "peak": ppeak,
+                                    "unit": "TFLOP/s", "frac": tf / ppeak,
+                                    "traffic": traffic_for("prefill.cu", "prefill_gptoss"),
+                                    "peak_source": peak_src}}
+            launches += psteps
+
+    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        cores = os.cpu_count() or 1
+        rows = np.arange(batch.batch_size, dtype=np.int64)
+        rr = np.repeat(rows, batch.num_qo_heads)
+        hh = np.tile(np.arange(batch.num_qo_heads, dtype=np.int32), len(rows))
+        t0 = time.perf_counter()
+        oracle.sink_attention(batch, rows=rr, heads=hh, n_threads=cores)
+        dt = time.perf_counter() - t0
+        cpu = {"value": bytes_step / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": f"the whole gptoss_decode batch (seed 0), fp64 C oracle, {dt:.2f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "gptoss_decode", "batch": batch.batch_size,
+                       "kv_len": "U[1024,8192]", "Hq": 64, "Hkv": 8, "head_dim": 64,
+                       "page_size": 16, "split_kv": True, "sinks": True,
+                       "kv_bytes_per_step": bytes_step, "l2": "flushed (256 MB memset) before every timed step",
+                       "parallelism": f"replicas x{world}", "plan_us": plan_us,
+                       "decode_units": units},
+            "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
+            "clocks": clocks, "cpu_baseline": cpu, "prefill": prefill,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup(args.impl)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,217 @@
+/*
+ * attn.h -- C ABI of libattn.so: batched GQA attention with a per-head sink
+ * logit over a paged KV cache, for one NVIDIA GB300 GPU (sm_103a).
+ *
+ * What is computed.  "GPT-OSS on day 0" (Perplexity), section "Sink
+ * Attention": every query head h owns one learned sink logit that takes part
+ * in the softmax.  It enters the denominator only (its value vector is zero)
+ * and is not multiplied by sm_scale:
+ *
+ *   out[i,h] = sum_j exp(s_ij - m) v_j / (sum_j exp(s_ij - m) + exp(sink_h - m))
+ *   s_ij     = sm_scale * q[i,h] . k_j            (k, v of KV head h / (Hq/Hkv))
+ *   lse[i,h] = m + ln(sum_j exp(s_ij - m) + exp(sink_h - m))   (natural log)
+ *
+ * The same section describes the kernels as parallel over heads and over the
+ * KV length, with the softmax computed online (running max and scale) and
+ * the sink placed in the first part of a KV split only; this library does
+ * exactly that (split-KV decode with a log-sum-exp merge).
+ *
+ * Request model, "Disaggregated prefill and decode" (Perplexity), section
+ * "Prefill vs decode performance": request b forwards qo_len_b query tokens
+ * and reads kv_len_b tokens from the KV cache; decode has qo_len = 1.  Query
+ * i of request b sits at absolute position kv_len_b - qo_len_b + i, so with
+ * causal masking it sees keys j <= kv_len_b - qo_len_b + i.
+ *
+ * KV cache layout, "Hosting Qwen on Blackwell" (Perplexity), section
+ * "Deploying on GB200 NVL72", and "Disaggregated prefill and decode", section
+ * "Sharded KV transfer": HND pages, heads outer and each page's tokens
+ * contiguous.  Concretely one pool, bf16, row-major:
+ *
+ *   kv_cache[num_pages][2][Hkv][page_size][head_dim]      ([.][0] = K, [.][1] = V)
+ *
+ * Tensors (all caller-owned device memory, row-major, contiguous):
+ *   q, out   bf16  [total_qo_rows][Hq][head_dim]   total_qo_rows = qo_indptr[batch]
+ *   lse      fp32  [total_qo_rows][Hq]             natural log; may be NULL
+ *   sinks    fp32  [Hq]                            may be NULL (no sink, i.e. -inf)
+ *
+ * Threading and streams: every launch is asynchronous on the caller's
+ * cudaStream_t, passed as void* (NULL = legacy default stream).  A plan may be
+ * used from one host thread at a time.  Launches that share a plan's
+ * workspace must not overlap on the GPU (issue them on one stream).
+ *
+ * Errors: functions return attn_status and never abort or throw.  Argument
+ * and shape checks happen on the host before anything is launched.  Kernels
+ * never trap: a page id outside the pool or a wait that runs out is recorded
+ * in a device error word of the plan's workspace (read it with
+ * attn_plan_device_error) and the offending load is skipped.
+ */
+#ifndef ATTN_H
+#define ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,          /* malformed pointer, size or index array */
+    ATTN_ERR_UNSUPPORTED = 2,          /* well-formed but outside the supported shapes */
+    ATTN_ERR_WORKSPACE_TOO_SMALL = 3,  /* bound workspace smaller than required */
+    ATTN_ERR_CUDA = 4,                 /* a CUDA runtime/driver call failed */
+    ATTN_ERR_NOT_BOUND = 5,            /* launch before attn_plan_bind_workspace */
+    ATTN_ERR_DEVICE = 6                /* a kernel recorded an error (see device error bits) */
+} attn_status;
+
+/* Bits of the device error word (attn_plan_device_error). */
+#define ATTN_DEVICE_ERR_PAGE_ID 1      /* page id outside [0, num_pages_in_pool) */
+#define ATTN_DEVICE_ERR_TIMEOUT 2      /* a bounded wait inside a kernel ran out */
+
+/* Opaque plan; owned by the library, freed with attn_plan_destroy. */
+typedef struct attn_plan_s* attn_plan_t;
+
+/* Summary of a plan (host-side copy, for callers and tests). */
+typedef struct {
+    int32_t batch;
+    int32_t total_qo_rows;
+    int32_t num_decode_requests;     /* requests with qo_len == 1 */
+    int32_t num_prefill_requests;    /* requests with qo_len > 1 */
+    int32_t num_decode_units;        /* CTAs of one attn_decode launch */
+    int32_t num_decode_groups_split; /* (request, kv head, head slice) groups split over >1 chunk */
+    int32_t num_decode_partials;     /* partial states held in the workspace */
+    int32_t decode_chunk_blocks;     /* target split-KV chunk, in 16-token blocks */
+    int32_t num_prefill_items;       /* CTAs of one attn_prefill launch */
+    int32_t num_sms;                 /* SM count the plan was balanced for */
+    int64_t decode_kv_tokens;        /* sum of kv_len over decode requests */
+    int64_t prefill_pairs;           /* visible (query, key) pairs over prefill rows, per query head */
+    size_t workspace_bytes;
+} attn_plan_info;
+
+/*
+ * attn_plan -- build the work list of one batch (host only; launches nothing).
+ *
+ * The split of the work over heads and over the KV length follows "GPT-OSS on
+ * day 0", section "Sink Attention"; the qo_len / kv_len request model follows
+ * "Disaggregated prefill and decode", section "Prefill vs decode performance".
+ * Requests with qo_len == 1 are decode requests (attn_decode), requests with
+ * qo_len > 1 are prefill requests (attn_prefill); qo_len == 0 contributes no
+ * rows.  Long decode sequences are split into chunks of whole 16-token blocks
+ * so that the number of CTAs fills num_sms SMs; chunk 0 of each split carries
+ * the sink and the chunks are merged by log-sum-exp inside the same launch.
+ *
+ *   qo_indptr      host int32 [batch+1]; qo_indptr[0] = 0, non-decreasing
+ *   kv_indptr      host int32 [batch+1]; CSR offsets of each request's pages in
+ *                  page_table; kv_indptr[0] = 0, non-decreasing
+ *   page_table     DEVICE int32 [kv_indptr[batch]]; page ids into the pool.
+ *                  Borrowed: it must stay valid, unchanged, for every launch
+ *                  made with this plan.  Not read by attn_plan.
+ *   last_page_len  host int32 [batch]; tokens used in the request's last page,
+ *                  1..page_size (ignored for a request with no pages);
+ *                  kv_len = (n_pages - 1) * page_size + last_page_len
+ *   batch >= 0; num_qo_heads % num_kv_heads == 0 (query head h reads KV head
+ *   h / (num_qo_heads / num_kv_heads)); head_dim in {64, 128}; page_size in
+ *   {16, 32, 64, 128}; qo_len <= kv_len for every request; causal in {0, 1};
+ *   sm_scale finite; num_pages_in_pool > 0 when any request has pages;
+ *   num_sms > 0, or 0 to query the current CUDA device.
+ *
+ * On success *plan_out owns host memory only and *workspace_bytes_out is the
+ * size of the device workspace the plan needs.  Nothing is written on error.
+ */
+ATTN_API attn_status attn_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
+                      const int32_t* page_table, const int32_t* last_page_len,
+                      int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads,
+                      int32_t head_dim, int32_t page_size, int32_t causal, float sm_scale,
+                      int32_t num_pages_in_pool, int32_t num_sms, attn_plan_t* plan_out,
+                      size_t* workspace_bytes_out);
+
+/*
+ * attn_plan_bind_workspace -- attach caller-owned device memory to the plan
+ * and upload the work list into it (asynchronous copy on `stream`; the host
+ * copy stays valid).  `workspace` must be 256-byte aligned and hold at least
+ * the plan's workspace_bytes; it is used by every later launch of the plan
+ * and must outlive them.  Clears the device error word and the split-merge
+ * counters.  May be called again (e.g. with other memory).
+ */
+ATTN_API attn_status attn_plan_bind_workspace(attn_plan_t plan, void* workspace, size_t bytes,
+                                     void* stream);
+
+/*
+ * attn_decode -- sink attention for the plan's decode rows (qo_len == 1):
+ * one CTA per (request, KV head, head slice, KV chunk); the GQA group's query
+ * heads share every K/V tile read from HBM.  Writes out and lse rows of
+ * decode requests only.  Pointers as in the file comment.
+ */
+ATTN_API attn_status attn_decode(attn_plan_t plan, const void* q, const void* kv_cache,
+                        const float* sinks, void* out, float* lse, void* stream);
+
+/*
+ * attn_prefill -- sink attention for the plan's prefill rows (qo_len > 1),
+ * causal or not as planned: one CTA per (128-row query tile, pair of query
+ * heads of one GQA group), QK^T and PV on the tensor cores.  Writes out and
+ * lse rows of prefill requests only.  For a mixed batch call attn_prefill
+ * and attn_decode with the same plan, in either order, on one stream.
+ */
+ATTN_API attn_status attn_prefill(attn_plan_t plan, const void* q, const void* kv_cache,
+                         const float* sinks, void* out, float* lse, void* stream);
+
+/*
+ * attn_merge_states -- combine two attention states over disjoint key sets
+ * into the state over their union, by the log-sum-exp rule implied by the
+ * split along the KV length in "GPT-OSS on day 0", section "Sink Attention"
+ * (the pages do not print it):
+ *   L = max(lse_a, lse_b);  w_x = exp(lse_x - L)
+ *   v_out = (w_a v_a + w_b v_b) / (w_a + w_b);  lse_out = L + ln(w_a + w_b)
+ * A state with lse = -inf (no keys, no sink) is the identity.  The sink must
+ * be counted in exactly one of the two inputs.
+ *
+ *   va, vb, vout   bf16 [n_tokens][n_heads][head_dim]  (vout may alias va or vb)
+ *   lsea, lseb     fp32 [n_tokens][n_heads], natural log
+ *   lseout         fp32 [n_tokens][n_heads] or NULL
+ *   head_dim a multiple of 4, at most 256.  Device pointers, async on stream.
+ */
+ATTN_API attn_status attn_merge_states(const void* va, const float* lsea, const void* vb,
+                              const float* lseb, void* vout, float* lseout, int32_t n_tokens,
+                              int32_t n_heads, int32_t head_dim, void* stream);
+
+/* Copy the plan's summary into *info (host only). */
+ATTN_API attn_status attn_plan_get_info(attn_plan_t plan, attn_plan_info* info);
+
+/*
+ * Host copies of the plan's work lists, for inspection and tests.  Each
+ * decode unit is 12 int32: q_row, page_base, kv_head, head0, n_heads,
+ * tok_begin, tok_end, chunk, n_chunks, group, partial0, reserved.  Each
+ * prefill item is 12 int32: q_row0, n_rows, page_base, kv_len, pos0, kv_head,
+ * head0, n_heads, n_kv_tiles, key_end, reserved, reserved (pos0 = absolute
+ * position of the tile's first query; key_end = one past the last key any
+ * row of the tile may see).  `capacity` counts units/items; at most that many
+ * are copied.
+ */
+ATTN_API attn_status attn_plan_get_decode_units(attn_plan_t plan, int32_t* units, int64_t capacity);
+ATTN_API attn_status attn_plan_get_prefill_items(attn_plan_t plan, int32_t* items, int64_t capacity);
+
+/*
+ * attn_plan_device_error -- wait for `stream`, then read and clear the plan's
+ * device error word (ATTN_DEVICE_ERR_* bits) into *code.  Returns
+ * ATTN_ERR_DEVICE if any bit was set.
+ */
+ATTN_API attn_status attn_plan_device_error(attn_plan_t plan, int32_t* code, void* stream);
+
+/* Free the plan's host memory.  Does not touch the workspace.  NULL is a no-op. */
+ATTN_API void attn_plan_destroy(attn_plan_t plan);
+
+/* Static, human-readable name of a status code. */
+ATTN_API const char* attn_status_string(attn_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_H */

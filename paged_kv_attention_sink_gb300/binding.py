@@ -1,0 +1,248 @@
+"""ctypes binding of libattn.so (argument marshalling only).
+
+Every step of the attention runs inside the library's CUDA kernels; this
+module checks tensor shapes / dtypes / devices, passes raw pointers and the
+current torch CUDA stream through the C ABI declared in ``include/attn.h``,
+and turns non-zero status codes into ``AttnError``.  There is no fallback:
+if the library is missing, importing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libattn.so")
+
+_STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "workspace too small",
+           4: "CUDA error", 5: "workspace not bound", 6: "device-side error recorded"}
+
+
+class AttnError(RuntimeError):
+    def __init__(self, fn: str, status: int, extra: str = ""):
+        self.status = status
+        super().__init__(f"{fn} failed: {_STATUS.get(status, status)}{extra}")
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("total_qo_rows", ctypes.c_int32),
+                ("num_decode_requests", ctypes.c_int32), ("num_prefill_requests", ctypes.c_int32),
+                ("num_decode_units", ctypes.c_int32), ("num_decode_groups_split", ctypes.c_int32),
+                ("num_decode_partials", ctypes.c_int32), ("decode_chunk_blocks", ctypes.c_int32),
+                ("num_prefill_items", ctypes.c_int32), ("num_sms", ctypes.c_int32),
+                ("decode_kv_tokens", ctypes.c_int64), ("prefill_pairs", ctypes.c_int64),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def _declare(lib):
+    p, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+    st = ctypes.c_int
+    sig = {
+        "attn_plan": (st, [p, p, p, p, i32, i32, i32, i32, i32, i32, f32, i32, i32, p, p]),
+        "attn_plan_bind_workspace": (st, [p, p, ctypes.c_size_t, p]),
+        "attn_decode": (st, [p, p, p, p, p, p, p]),
+        "attn_prefill": (st, [p, p, p, p, p, p, p]),
+        "attn_merge_states": (st, [p, p, p, p, p, p, i32, i32, i32, p]),
+        "attn_plan_get_info": (st, [p, p]),
+        "attn_plan_get_decode_units": (st, [p, p, i64]),
+        "attn_plan_get_prefill_items": (st, [p, p, i64]),
+        "attn_plan_device_error": (st, [p, p, p]),
+        "attn_plan_destroy": (None, [p]),
+        "attn_status_string": (ctypes.c_char_p, [st]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = None
+
+
+def load_library():
+    """Load libattn.so (raises ImportError if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise ImportError(f"{_LIB_PATH} is missing: build it with "
+                              "`python -c 'import __graft_entry__ as g; g.build()'`")
+        _lib = _declare(ctypes.CDLL(_LIB_PATH))
+    return _lib
+
+
+load_library()
+
+
+def _check(fn: str, status: int, extra: str = ""):
+    if status != 0:
+        raise AttnError(fn, status, extra)
+
+
+def _i32_host(a) -> np.ndarray:
+    if isinstance(a, torch.Tensor):
+        a = a.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(a), dtype=np.int32)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+class Plan:
+    """A planned batch: host work lists inside the library plus the device
+    workspace (a torch uint8 buffer) they were uploaded to.
+
+    qo_indptr, kv_indptr, last_page_len: host int arrays (or CPU tensors).
+    page_table: int32 CUDA tensor; kept referenced by the plan.
+    """
+
+    def __init__(self, qo_indptr, kv_indptr, page_table: torch.Tensor, last_page_len,
+                 num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
+                 causal: bool = True, sm_scale: Optional[float] = None,
+                 num_pages: Optional[int] = None, num_sms: int = 0, stream=None):
+        lib = load_library()
+        self._handle = None
+        qo = _i32_host(qo_indptr)
+        kv = _i32_host(kv_indptr)
+        lpl = _i32_host(last_page_len)
+        if not (isinstance(page_table, torch.Tensor) and page_table.is_cuda and
+                page_table.dtype == torch.int32 and page_table.is_contiguous()):
+            raise TypeError("page_table must be a contiguous int32 CUDA tensor")
+        if num_pages is None:
+            raise ValueError("num_pages (pages in the KV pool) is required")
+        self.page_table = page_table
+        self.batch = len(qo) - 1
+        self.num_qo_heads, self.num_kv_heads = num_qo_heads, num_kv_heads
+        self.head_dim, self.page_size, self.num_pages = head_dim, page_size, num_pages
+        self.causal = bool(causal)
+        self.sm_scale = float(sm_scale) if sm_scale is not None else head_dim ** -0.5
+        self.total_rows = int(qo[-1]) if len(qo) else 0
+        handle = ctypes.c_void_p()
+        ws_bytes = ctypes.c_size_t()
+        _check("attn_plan", lib.attn_plan(
+            qo.ctypes.data_as(ctypes.c_void_p), kv.ctypes.data_as(ctypes.c_void_p),
+            _ptr(page_table), lpl.ctypes.data_as(ctypes.c_void_p), self.batch, num_qo_heads,
+            num_kv_heads, head_dim, page_size, int(self.causal), self.sm_scale, int(num_pages),
+            int(num_sms), ctypes.byref(handle), ctypes.byref(ws_bytes)))
+        self._handle = handle
+        self.workspace = torch.empty(max(int(ws_bytes.value), 256), dtype=torch.uint8,
+                                     device=page_table.device)
+        _check("attn_plan_bind_workspace", lib.attn_plan_bind_workspace(
+            self._handle, _ptr(self.workspace), self.workspace.numel(), _stream_ptr(stream)))
+
+    def __del__(self):
+        if getattr(self, "_handle", None) is not None and _lib is not None:
+            _lib.attn_plan_destroy(self._handle)
+            self._handle = None
+
+    @property
+    def handle(self):
+        return self._handle
+
+    def info(self) -> dict:
+        info = PlanInfo()
+        _check("attn_plan_get_info", load_library().attn_plan_get_info(self._handle, ctypes.byref(info)))
+        return info.as_dict()
+
+    def decode_units(self) -> np.ndarray:
+        n = self.info()["num_decode_units"]
+        out = np.zeros((n, 12), dtype=np.int32)
+        _check("attn_plan_get_decode_units", load_library().attn_plan_get_decode_units(
+            self._handle, out.ctypes.data_as(ctypes.c_void_p), n))
+        return out
+
+    def prefill_items(self) -> np.ndarray:
+        n = self.info()["num_prefill_items"]
+        out = np.zeros((n, 12), dtype=np.int32)
+        _check("attn_plan_get_prefill_items", load_library().attn_plan_get_prefill_items(
+            self._handle, out.ctypes.data_as(ctypes.c_void_p), n))
+        return out
+
+    def device_error(self, stream=None) -> int:
+        code = ctypes.c_int32()
+        status = load_library().attn_plan_device_error(self._handle, ctypes.byref(code), _stream_ptr(stream))
+        if status not in (0, 6):
+            _check("attn_plan_device_error", status)
+        return int(code.value)
+
+    # -- launches ---------------------------------------------------------
+    def _check_tensors(self, q, kv_cache, sinks, out, lse):
+        H, D = self.num_qo_heads, self.head_dim
+        for name, t, dt in (("q", q, torch.bfloat16), ("kv_cache", kv_cache, torch.bfloat16),
+                            ("out", out, torch.bfloat16)):
+            if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == dt and t.is_contiguous()):
+                raise TypeError(f"{name} must be a contiguous {dt} CUDA tensor")
+        if tuple(q.shape) != (self.total_rows, H, D) or tuple(out.shape) != (self.total_rows, H, D):
+            raise ValueError(f"q / out must be [{self.total_rows}, {H}, {D}]")
+        if tuple(kv_cache.shape) != (self.num_pages, 2, self.num_kv_heads, self.page_size, D):
+            raise ValueError("kv_cache must be [num_pages, 2, Hkv, page_size, head_dim]")
+        if sinks is not None and not (sinks.is_cuda and sinks.dtype == torch.float32 and
+                                      sinks.is_contiguous() and sinks.numel() == H):
+            raise TypeError("sinks must be a contiguous float32 CUDA tensor of num_qo_heads values")
+        if lse is not None and not (lse.is_cuda and lse.dtype == torch.float32 and lse.is_contiguous()
+                                    and tuple(lse.shape) == (self.total_rows, H)):
+            raise TypeError("lse must be a contiguous float32 CUDA tensor [rows, Hq]")
+
+    def _launch(self, fn_name, q, kv_cache, sinks, out, lse, stream):
+        self._check_tensors(q, kv_cache, sinks, out, lse)
+        fn = getattr(load_library(), fn_name)
+        _check(fn_name, fn(self._handle, _ptr(q), _ptr(kv_cache), _ptr(sinks), _ptr(out), _ptr(lse),
+                           _stream_ptr(stream)))
+        return out, lse
+
+    def decode(self, q, kv_cache, sinks=None, out=None, lse=None, stream=None):
+        out = torch.empty_like(q) if out is None else out
+        return self._launch("attn_decode", q, kv_cache, sinks, out, lse, stream)
+
+    def prefill(self, q, kv_cache, sinks=None, out=None, lse=None, stream=None):
+        out = torch.empty_like(q) if out is None else out
+        return self._launch("attn_prefill", q, kv_cache, sinks, out, lse, stream)
+
+
+def attn_plan(qo_indptr, kv_indptr, page_table, last_page_len, num_qo_heads, num_kv_heads,
+              head_dim, page_size, causal=True, sm_scale=None, num_pages=None, num_sms=0,
+              stream=None) -> Plan:
+    return Plan(qo_indptr, kv_indptr, page_table, last_page_len, num_qo_heads, num_kv_heads,
+                head_dim, page_size, causal=causal, sm_scale=sm_scale, num_pages=num_pages,
+                num_sms=num_sms, stream=stream)
+
+
+def attn_decode(plan: Plan, q, kv_cache, sinks=None, out=None, lse=None, stream=None):
+    return plan.decode(q, kv_cache, sinks, out, lse, stream)
+
+
+def attn_prefill(plan: Plan, q, kv_cache, sinks=None, out=None, lse=None, stream=None):
+    return plan.prefill(q, kv_cache, sinks, out, lse, stream)
+
+
+def attn_merge_states(va, lsea, vb, lseb, vout=None, lseout=None, stream=None):
+    """Merge two (bf16 [n, H, D], fp32 [n, H]) attention states by log-sum-exp."""
+    for name, t, dt in (("va", va, torch.bfloat16), ("vb", vb, torch.bfloat16),
+                        ("lsea", lsea, torch.float32), ("lseb", lseb, torch.float32)):
+        if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == dt and t.is_contiguous()):
+            raise TypeError(f"{name} must be a contiguous {dt} CUDA tensor")
+    n, H, D = va.shape
+    if vb.shape != va.shape or lsea.shape != (n, H) or lseb.shape != (n, H):
+        raise ValueError("state shapes disagree")
+    vout = torch.empty_like(va) if vout is None else vout
+    _check("attn_merge_states", load_library().attn_merge_states(
+        _ptr(va), _ptr(lsea), _ptr(vb), _ptr(lseb), _ptr(vout), _ptr(lseout), n, H, D,
+        _stream_ptr(stream)))
+    return vout, lseout

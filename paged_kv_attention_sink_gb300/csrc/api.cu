@@ -1,0 +1,155 @@
+// C entry points of libattn.so: argument checks, workspace binding, TMA
+// descriptor construction, and dispatch to the kernel launchers.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "attn_internal.h"
+#include "kernels.h"
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &qr) == cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// The HND pool as a 3-D tensor {dim, token in page, (page, K/V, KV head)}:
+// one box is `box_rows` consecutive tokens x 64 dims of one (page, KV head)
+// block of K or V, stored 128-byte swizzled.
+bool make_kv_map(void* map, const void* kv, const attn_plan_s* p, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)p->D, (cuuint64_t)p->P, (cuuint64_t)p->num_pages * 2 * p->Hkv};
+    cuuint64_t strides[2] = {(cuuint64_t)p->D * 2, (cuuint64_t)p->P * p->D * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+    cuuint32_t elem[3] = {1, 1, 1};
+    return fn(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+              const_cast<void*>(kv), dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// q [rows][Hq][D] as a 3-D tensor {dim, head, row}: one box is 128 rows x 64
+// dims of one head; rows past the end read as zero.
+bool make_q_map(void* map, const void* q, const attn_plan_s* p) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const int64_t rows = p->info.total_qo_rows;
+    cuuint64_t dims[3] = {(cuuint64_t)p->D, (cuuint64_t)p->Hq, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)p->D * 2, (cuuint64_t)p->Hq * p->D * 2};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)attn::kPrefillRows};
+    cuuint32_t elem[3] = {1, 1, 1};
+    return fn(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+              const_cast<void*>(q), dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+attn_status check_launch(attn_plan_t plan, const void* q, const void* kv, const void* out) {
+    if (!plan) return ATTN_ERR_INVALID_ARG;
+    if (!plan->bound) return ATTN_ERR_NOT_BOUND;
+    if (!q || !kv || !out) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(kv) || !aligned16(out)) return ATTN_ERR_INVALID_ARG;
+    return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" attn_status attn_plan_bind_workspace(attn_plan_t plan, void* workspace, size_t bytes,
+                                                void* stream) {
+    if (!plan) return ATTN_ERR_INVALID_ARG;
+    const attn::WorkspaceLayout& L = plan->layout;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return ATTN_ERR_INVALID_ARG;
+    if (bytes < L.total) return ATTN_ERR_WORKSPACE_TOO_SMALL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    if (!plan->units.empty() &&
+        cudaMemcpyAsync(ws + L.units, plan->units.data(), plan->units.size() * sizeof(attn::DecodeUnit),
+                        cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    if (!plan->items.empty() &&
+        cudaMemcpyAsync(ws + L.items, plan->items.data(), plan->items.size() * sizeof(attn::PrefillItem),
+                        cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    // counters and the error word are adjacent: clear both.
+    if (cudaMemsetAsync(ws + L.counters, 0, L.part_lse - L.counters, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    plan->ws = ws;
+    plan->ws_bytes = bytes;
+    plan->bound = true;
+    return ATTN_OK;
+}
+
+extern "C" attn_status attn_decode(attn_plan_t plan, const void* q, const void* kv_cache,
+                                   const float* sinks, void* out, float* lse, void* stream) {
+    if (plan && plan->bound && plan->units.empty()) return ATTN_OK;
+    attn_status st = check_launch(plan, q, kv_cache, out);
+    if (st != ATTN_OK) return st;
+    if (plan->kv_map_decode_ptr != kv_cache) {
+        if (!make_kv_map(plan->kv_map_decode, kv_cache, plan, attn::kBlockTokens)) return ATTN_ERR_CUDA;
+        plan->kv_map_decode_ptr = kv_cache;
+    }
+    return attn::launch_decode(plan, q, plan->kv_map_decode, sinks, out, lse,
+                               static_cast<cudaStream_t>(stream));
+}
+
+extern "C" attn_status attn_prefill(attn_plan_t plan, const void* q, const void* kv_cache,
+                                    const float* sinks, void* out, float* lse, void* stream) {
+    if (plan && plan->bound && plan->items.empty()) return ATTN_OK;
+    attn_status st = check_launch(plan, q, kv_cache, out);
+    if (st != ATTN_OK) return st;
+    if (plan->kv_map_prefill_ptr != kv_cache) {
+        const int box = plan->P < attn::kPrefillKeys ? plan->P : attn::kPrefillKeys;
+        if (!make_kv_map(plan->kv_map_prefill, kv_cache, plan, box)) return ATTN_ERR_CUDA;
+        plan->kv_map_prefill_ptr = kv_cache;
+    }
+    if (plan->q_map_prefill_ptr != q) {
+        if (!make_q_map(plan->q_map_prefill, q, plan)) return ATTN_ERR_CUDA;
+        plan->q_map_prefill_ptr = q;
+    }
+    return attn::launch_prefill(plan, plan->q_map_prefill, plan->kv_map_prefill, sinks, out, lse,
+                                static_cast<cudaStream_t>(stream));
+}
+
+extern "C" attn_status attn_merge_states(const void* va, const float* lsea, const void* vb,
+                                         const float* lseb, void* vout, float* lseout,
+                                         int32_t n_tokens, int32_t n_heads, int32_t head_dim,
+                                         void* stream) {
+    if (n_tokens < 0 || n_heads <= 0 || head_dim <= 0 || head_dim % 4 != 0 || head_dim > 256)
+        return ATTN_ERR_INVALID_ARG;
+    if (n_tokens == 0) return ATTN_OK;
+    if (!va || !lsea || !vb || !lseb || !vout) return ATTN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(va) | reinterpret_cast<uintptr_t>(vb) |
+         reinterpret_cast<uintptr_t>(vout)) & 7)
+        return ATTN_ERR_INVALID_ARG;
+    return attn::launch_merge_states(va, lsea, vb, lseb, vout, lseout, (int64_t)n_tokens * n_heads,
+                                     head_dim, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" attn_status attn_plan_device_error(attn_plan_t plan, int32_t* code, void* stream) {
+    if (!plan || !code) return ATTN_ERR_INVALID_ARG;
+    if (!plan->bound) return ATTN_ERR_NOT_BOUND;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t v = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (cudaMemcpy(&v, plan->ws + plan->layout.err, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    if (v != 0 && cudaMemset(plan->ws + plan->layout.err, 0, sizeof v) != cudaSuccess) return ATTN_ERR_CUDA;
+    *code = v;
+    return v != 0 ? ATTN_ERR_DEVICE : ATTN_OK;
+}

@@ -1,0 +1,92 @@
+// Internal declarations shared by the planner (host) and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <vector>
+
+#include "../../include/attn.h"
+
+namespace attn {
+
+constexpr int kBlockTokens = 16;          // decode streams K/V in 16-token blocks
+constexpr int kMaxSliceHeads = 16;        // query heads per decode CTA (one m16 MMA tile)
+constexpr int kDecodeWarps = 4;           // warps per decode CTA
+constexpr int kDecodeMinChunkBlocks = 8;  // never split a sequence finer than 128 tokens
+constexpr int kDecodeMaxChunkBlocks = 512;
+constexpr int kDecodeMaxChunkPages = kDecodeMaxChunkBlocks * kBlockTokens / 16 + 2;
+constexpr int kPrefillRows = 128;         // query rows per prefill tile (TMEM lanes)
+constexpr int kPrefillKeys = 128;         // keys per prefill KV tile
+
+// One decode CTA: a chunk [tok_begin, tok_end) of one request's KV sequence for
+// one KV head and up to 16 of its query heads.
+struct DecodeUnit {
+    int32_t q_row;      // row of q / out / lse
+    int32_t page_base;  // kv_indptr[b]: first slot of the request in page_table
+    int32_t kv_head;
+    int32_t head0;      // first query head of the slice
+    int32_t n_heads;    // query heads in the slice (1..16)
+    int32_t tok_begin;  // a multiple of 16
+    int32_t tok_end;    // <= kv_len
+    int32_t chunk;      // index of this chunk within its group; chunk 0 carries the sink
+    int32_t n_chunks;   // 1 = not split
+    int32_t group;      // split-merge counter index, -1 when not split
+    int32_t partial0;   // first partial-state slot of the group
+    int32_t reserved;
+};
+static_assert(sizeof(DecodeUnit) == 48, "decode unit is 12 int32");
+
+// One prefill CTA: 128 query rows of one request for up to two query heads of
+// one GQA group.
+struct PrefillItem {
+    int32_t q_row0;      // first row of the tile in q / out / lse
+    int32_t n_rows;      // valid rows (1..128)
+    int32_t page_base;
+    int32_t kv_len;
+    int32_t pos0;        // absolute position of row 0 (kv_len - qo_len + tile offset)
+    int32_t kv_head;
+    int32_t head0;
+    int32_t n_heads;     // 1 or 2
+    int32_t n_kv_tiles;  // 128-key tiles visited
+    int32_t key_end;     // one past the last key any row of the tile may see
+    int32_t reserved0;
+    int32_t reserved1;
+};
+static_assert(sizeof(PrefillItem) == 48, "prefill item is 12 int32");
+
+struct WorkspaceLayout {
+    size_t units = 0, items = 0, counters = 0, err = 0, part_lse = 0, part_o = 0, total = 0;
+};
+
+// CTAs of the decode kernel resident per SM for a head dim (matches its
+// shared-memory footprint); defined next to the kernel.
+int decode_ctas_per_sm(int head_dim);
+
+}  // namespace attn
+
+struct attn_plan_s {
+    int32_t batch = 0, Hq = 0, Hkv = 0, D = 0, P = 0, causal = 0;
+    float sm_scale = 0.f;
+    int32_t num_pages = 0;
+    int32_t num_sms = 0;
+    const int32_t* page_table = nullptr;  // device, borrowed
+
+    std::vector<attn::DecodeUnit> units;
+    std::vector<attn::PrefillItem> items;
+    int32_t n_groups = 0;
+    int32_t n_partials = 0;
+    attn_plan_info info{};
+    attn::WorkspaceLayout layout;
+
+    unsigned char* ws = nullptr;  // device, caller-owned
+    size_t ws_bytes = 0;
+    bool bound = false;
+
+    // Tensor maps are 128-byte opaque driver objects; cached per KV / Q pointer.
+    alignas(64) unsigned char kv_map_decode[128];
+    const void* kv_map_decode_ptr = nullptr;
+    alignas(64) unsigned char kv_map_prefill[128];
+    const void* kv_map_prefill_ptr = nullptr;
+    alignas(64) unsigned char q_map_prefill[128];
+    const void* q_map_prefill_ptr = nullptr;
+};

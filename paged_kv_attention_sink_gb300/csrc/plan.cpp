@@ -1,0 +1,243 @@
+// Host-side work planner: turns one ragged batch into the decode units and
+// prefill items the kernels run, and lays out the device workspace.
+//
+// Work is spread over heads and over the KV length ("GPT-OSS on day 0",
+// section "Sink Attention"); the cost of a request grows with kv_len for both
+// prefill and decode ("Disaggregated prefill and decode", section "Prefill vs
+// decode performance"), so decode sequences are cut into chunks of similar
+// size until the CTAs fill the GPU, and both lists are ordered longest first.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <new>
+
+#include <cuda_runtime.h>
+
+#include "attn_internal.h"
+
+namespace {
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool supported_head_dim(int d) { return d == 64 || d == 128; }
+bool supported_page_size(int p) { return p == 16 || p == 32 || p == 64 || p == 128; }
+
+}  // namespace
+
+extern "C" attn_status attn_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
+                                 const int32_t* page_table, const int32_t* last_page_len,
+                                 int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads,
+                                 int32_t head_dim, int32_t page_size, int32_t causal,
+                                 float sm_scale, int32_t num_pages_in_pool, int32_t num_sms,
+                                 attn_plan_t* plan_out, size_t* workspace_bytes_out) {
+    using namespace attn;
+    if (!plan_out || !workspace_bytes_out || batch < 0) return ATTN_ERR_INVALID_ARG;
+    if (batch > 0 && (!qo_indptr || !kv_indptr || !last_page_len)) return ATTN_ERR_INVALID_ARG;
+    if (num_qo_heads <= 0 || num_kv_heads <= 0 || num_qo_heads % num_kv_heads != 0)
+        return ATTN_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+    if (!std::isfinite(sm_scale)) return ATTN_ERR_INVALID_ARG;
+    if (head_dim <= 0 || page_size <= 0 || num_sms < 0) return ATTN_ERR_INVALID_ARG;
+    if (!supported_head_dim(head_dim) || !supported_page_size(page_size)) return ATTN_ERR_UNSUPPORTED;
+
+    // Validate the index arrays and derive kv_len.
+    std::vector<int64_t> qo_len(batch), kv_len(batch);
+    if (batch > 0 && (qo_indptr[0] != 0 || kv_indptr[0] != 0)) return ATTN_ERR_INVALID_ARG;
+    int64_t total_pages = 0;
+    for (int32_t b = 0; b < batch; ++b) {
+        int64_t nq = (int64_t)qo_indptr[b + 1] - qo_indptr[b];
+        int64_t np = (int64_t)kv_indptr[b + 1] - kv_indptr[b];
+        if (nq < 0 || np < 0) return ATTN_ERR_INVALID_ARG;
+        int64_t kv = 0;
+        if (np > 0) {
+            if (last_page_len[b] < 1 || last_page_len[b] > page_size) return ATTN_ERR_INVALID_ARG;
+            kv = (np - 1) * page_size + last_page_len[b];
+        }
+        if (nq > kv) return ATTN_ERR_INVALID_ARG;
+        if (kv > (int64_t)INT32_MAX / 2) return ATTN_ERR_UNSUPPORTED;
+        qo_len[b] = nq;
+        kv_len[b] = kv;
+        total_pages += np;
+    }
+    if (total_pages > 0 && (!page_table || num_pages_in_pool <= 0)) return ATTN_ERR_INVALID_ARG;
+    const int64_t total_rows = batch > 0 ? qo_indptr[batch] : 0;
+    if (total_rows * num_qo_heads > (int64_t)INT32_MAX) return ATTN_ERR_UNSUPPORTED;
+
+    if (num_sms == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return ATTN_ERR_CUDA;
+        }
+    }
+
+    attn_plan_s* plan = new (std::nothrow) attn_plan_s();
+    if (!plan) return ATTN_ERR_INVALID_ARG;
+    plan->batch = batch;
+    plan->Hq = num_qo_heads;
+    plan->Hkv = num_kv_heads;
+    plan->D = head_dim;
+    plan->P = page_size;
+    plan->causal = causal;
+    plan->sm_scale = sm_scale;
+    plan->num_pages = num_pages_in_pool;
+    plan->num_sms = num_sms;
+    plan->page_table = page_table;
+
+    const int G = num_qo_heads / num_kv_heads;
+    const int n_slices = (G + kMaxSliceHeads - 1) / kMaxSliceHeads;
+
+    // ---- decode: chunk size so that the units fill about two waves of CTAs.
+    int64_t total_blocks = 0;
+    int32_t n_decode = 0, n_prefill = 0;
+    int64_t decode_tokens = 0, prefill_pairs = 0;
+    for (int32_t b = 0; b < batch; ++b) {
+        if (qo_len[b] == 1) {
+            ++n_decode;
+            decode_tokens += kv_len[b];
+            total_blocks += (kv_len[b] + kBlockTokens - 1) / kBlockTokens * num_kv_heads * n_slices;
+        } else if (qo_len[b] > 1) {
+            ++n_prefill;
+        }
+    }
+    const int64_t slots = (int64_t)num_sms * decode_ctas_per_sm(head_dim);
+    const int64_t target_units = std::max<int64_t>(1, 2 * slots);
+    int64_t chunk = (total_blocks + target_units - 1) / target_units;
+    chunk = std::min<int64_t>(std::max<int64_t>(chunk, kDecodeMinChunkBlocks), kDecodeMaxChunkBlocks);
+
+    for (int32_t b = 0; b < batch; ++b) {
+        if (qo_len[b] != 1) continue;
+        const int64_t nblk = (kv_len[b] + kBlockTokens - 1) / kBlockTokens;
+        int64_t n_chunks = std::max<int64_t>(1, (nblk + chunk / 2) / chunk);
+        n_chunks = std::max<int64_t>(n_chunks, (nblk + kDecodeMaxChunkBlocks - 1) / kDecodeMaxChunkBlocks);
+        for (int32_t g = 0; g < num_kv_heads; ++g) {
+            for (int s = 0; s < n_slices; ++s) {
+                int32_t group = -1, partial0 = 0;
+                if (n_chunks > 1) {
+                    group = plan->n_groups++;
+                    partial0 = plan->n_partials;
+                    plan->n_partials += (int32_t)n_chunks;
+                }
+                for (int64_t c = 0; c < n_chunks; ++c) {
+                    const int64_t blk0 = c * nblk / n_chunks, blk1 = (c + 1) * nblk / n_chunks;
+                    DecodeUnit u{};
+                    u.q_row = qo_indptr[b];
+                    u.page_base = kv_indptr[b];
+                    u.kv_head = g;
+                    u.head0 = g * G + s * kMaxSliceHeads;
+                    u.n_heads = std::min(kMaxSliceHeads, G - s * kMaxSliceHeads);
+                    u.tok_begin = (int32_t)(blk0 * kBlockTokens);
+                    u.tok_end = (int32_t)std::min<int64_t>(kv_len[b], blk1 * kBlockTokens);
+                    u.chunk = (int32_t)c;
+                    u.n_chunks = (int32_t)n_chunks;
+                    u.group = group;
+                    u.partial0 = partial0;
+                    plan->units.push_back(u);
+                }
+            }
+        }
+    }
+    std::stable_sort(plan->units.begin(), plan->units.end(),
+                     [](const DecodeUnit& a, const DecodeUnit& b) {
+                         return (a.tok_end - a.tok_begin) > (b.tok_end - b.tok_begin);
+                     });
+
+    // ---- prefill: one item per (128-row tile, pair of query heads of a group).
+    for (int32_t b = 0; b < batch; ++b) {
+        if (qo_len[b] <= 1) continue;
+        const int64_t prefix = kv_len[b] - qo_len[b];
+        for (int64_t r = 0; r < qo_len[b]; ++r)
+            prefill_pairs += causal ? (prefix + r + 1) : kv_len[b];
+        for (int64_t t0 = 0; t0 < qo_len[b]; t0 += kPrefillRows) {
+            const int32_t rows = (int32_t)std::min<int64_t>(kPrefillRows, qo_len[b] - t0);
+            const int64_t pos0 = prefix + t0;
+            const int64_t key_end = causal ? std::min<int64_t>(kv_len[b], pos0 + rows) : kv_len[b];
+            for (int32_t g = 0; g < num_kv_heads; ++g) {
+                for (int hp = 0; hp < G; hp += 2) {
+                    PrefillItem it{};
+                    it.q_row0 = (int32_t)(qo_indptr[b] + t0);
+                    it.n_rows = rows;
+                    it.page_base = kv_indptr[b];
+                    it.kv_len = (int32_t)kv_len[b];
+                    it.pos0 = (int32_t)pos0;
+                    it.kv_head = g;
+                    it.head0 = g * G + hp;
+                    it.n_heads = std::min(2, G - hp);
+                    it.n_kv_tiles = (int32_t)((key_end + kPrefillKeys - 1) / kPrefillKeys);
+                    it.key_end = (int32_t)key_end;
+                    plan->items.push_back(it);
+                }
+            }
+        }
+    }
+    std::stable_sort(plan->items.begin(), plan->items.end(),
+                     [](const PrefillItem& a, const PrefillItem& b) {
+                         return a.n_kv_tiles * a.n_heads > b.n_kv_tiles * b.n_heads;
+                     });
+
+    // ---- workspace layout (every region 256-byte aligned).
+    WorkspaceLayout& L = plan->layout;
+    size_t off = 0;
+    L.units = off;    off = align_up(off + plan->units.size() * sizeof(DecodeUnit), 256);
+    L.items = off;    off = align_up(off + plan->items.size() * sizeof(PrefillItem), 256);
+    L.counters = off; off = align_up(off + (size_t)plan->n_groups * sizeof(int32_t), 256);
+    L.err = off;      off = align_up(off + sizeof(int32_t), 256);
+    L.part_lse = off; off = align_up(off + (size_t)plan->n_partials * kMaxSliceHeads * sizeof(float), 256);
+    L.part_o = off;   off = align_up(off + (size_t)plan->n_partials * kMaxSliceHeads * head_dim * sizeof(float), 256);
+    L.total = off;
+
+    attn_plan_info& I = plan->info;
+    I.batch = batch;
+    I.total_qo_rows = (int32_t)total_rows;
+    I.num_decode_requests = n_decode;
+    I.num_prefill_requests = n_prefill;
+    I.num_decode_units = (int32_t)plan->units.size();
+    I.num_decode_groups_split = plan->n_groups;
+    I.num_decode_partials = plan->n_partials;
+    I.decode_chunk_blocks = (int32_t)chunk;
+    I.num_prefill_items = (int32_t)plan->items.size();
+    I.num_sms = num_sms;
+    I.decode_kv_tokens = decode_tokens;
+    I.prefill_pairs = prefill_pairs;
+    I.workspace_bytes = L.total;
+
+    *plan_out = plan;
+    *workspace_bytes_out = L.total;
+    return ATTN_OK;
+}
+
+extern "C" attn_status attn_plan_get_info(attn_plan_t plan, attn_plan_info* info) {
+    if (!plan || !info) return ATTN_ERR_INVALID_ARG;
+    *info = plan->info;
+    return ATTN_OK;
+}
+
+extern "C" attn_status attn_plan_get_decode_units(attn_plan_t plan, int32_t* units, int64_t capacity) {
+    if (!plan || (!units && capacity > 0) || capacity < 0) return ATTN_ERR_INVALID_ARG;
+    const int64_t n = std::min<int64_t>(capacity, (int64_t)plan->units.size());
+    if (n > 0) std::memcpy(units, plan->units.data(), (size_t)n * sizeof(attn::DecodeUnit));
+    return ATTN_OK;
+}
+
+extern "C" attn_status attn_plan_get_prefill_items(attn_plan_t plan, int32_t* items, int64_t capacity) {
+    if (!plan || (!items && capacity > 0) || capacity < 0) return ATTN_ERR_INVALID_ARG;
+    const int64_t n = std::min<int64_t>(capacity, (int64_t)plan->items.size());
+    if (n > 0) std::memcpy(items, plan->items.data(), (size_t)n * sizeof(attn::PrefillItem));
+    return ATTN_OK;
+}
+
+extern "C" void attn_plan_destroy(attn_plan_t plan) { delete plan; }
+
+extern "C" const char* attn_status_string(attn_status status) {
+    switch (status) {
+        case ATTN_OK: return "ok";
+        case ATTN_ERR_INVALID_ARG: return "invalid argument";
+        case ATTN_ERR_UNSUPPORTED: return "unsupported shape";
+        case ATTN_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case ATTN_ERR_CUDA: return "CUDA error";
+        case ATTN_ERR_NOT_BOUND: return "workspace not bound";
+        case ATTN_ERR_DEVICE: return "device-side error recorded";
+    }
+    return "unknown status";
+}

@@ -1,0 +1,207 @@
+"""CPU checks of the C ABI: the library loads, exports every symbol that
+include/attn.h declares, and the host planner builds correct work lists and
+rejects malformed input with status codes (no GPU needed: attn_plan never
+touches the device when num_sms is given, and never reads page_table)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+OK, INVALID, UNSUPPORTED = 0, 1, 2
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_attention_sink_gb300 import build
+    build.build()
+    from paged_kv_attention_sink_gb300 import binding
+    return binding.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"ATTN_API\s+[\w\s\*]+?\b(attn_\w+)\s*\(", text)
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 11
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert lib.attn_status_string(code)
+    assert lib.attn_status_string(0) == b"ok"
+
+
+FAKE_PT = ctypes.c_void_p(0x1000)   # never dereferenced by the planner
+
+
+def plan(lib, qo, kv_pages, last, Hq=64, Hkv=8, D=64, P=16, causal=1, pool=100000, sms=152):
+    qo_indptr = np.concatenate([[0], np.cumsum(qo)]).astype(np.int32)
+    kv_indptr = np.concatenate([[0], np.cumsum(kv_pages)]).astype(np.int32)
+    last = np.asarray(last, dtype=np.int32)
+    handle = ctypes.c_void_p()
+    ws = ctypes.c_size_t()
+    st = lib.attn_plan(qo_indptr.ctypes.data_as(ctypes.c_void_p), kv_indptr.ctypes.data_as(ctypes.c_void_p),
+                       FAKE_PT, last.ctypes.data_as(ctypes.c_void_p), len(qo), Hq, Hkv, D, P, causal,
+                       D ** -0.5, pool, sms, ctypes.byref(handle), ctypes.byref(ws))
+    return st, handle, ws.value
+
+
+def units_of(lib, handle):
+    from paged_kv_attention_sink_gb300.binding import PlanInfo
+    info = PlanInfo()
+    assert lib.attn_plan_get_info(handle, ctypes.byref(info)) == OK
+    u = np.zeros((info.num_decode_units, 12), dtype=np.int32)
+    assert lib.attn_plan_get_decode_units(handle, u.ctypes.data_as(ctypes.c_void_p), len(u)) == OK
+    it = np.zeros((info.num_prefill_items, 12), dtype=np.int32)
+    assert lib.attn_plan_get_prefill_items(handle, it.ctypes.data_as(ctypes.c_void_p), len(it)) == OK
+    return info, u, it
+
+
+@pytest.mark.parametrize("Hq,Hkv,P", [(64, 8, 16), (64, 4, 64), (8, 2, 16), (48, 1, 32), (20, 20, 128)])
+def test_decode_units_cover_every_token_once(lib, Hq, Hkv, P):
+    rng = np.random.default_rng(Hq + P)
+    kv = rng.integers(1, 20000, size=37)
+    pages = (kv + P - 1) // P
+    last = kv - (pages - 1) * P
+    st, h, ws = plan(lib, [1] * len(kv), pages, last, Hq=Hq, Hkv=Hkv, P=P)
+    assert st == OK and ws > 0
+    info, u, _ = units_of(lib, h)
+    G = Hq // Hkv
+    cover = {}
+    for (q_row, page_base, g, head0, nh, t0, t1, chunk, nch, group, part0, _) in u:
+        assert t0 % 16 == 0 and t0 < t1 and nh >= 1 and nh <= 16
+        assert head0 >= g * G and head0 + nh <= (g + 1) * G
+        assert (t1 - t0) <= 512 * 16
+        assert (group >= 0) == (nch > 1)
+        for hh in range(head0, head0 + nh):
+            cover.setdefault((q_row, hh), []).append((t0, t1, chunk, nch))
+    assert len(cover) == len(kv) * Hq
+    for b in range(len(kv)):
+        for hh in range(Hq):
+            parts = sorted(cover[(b, hh)])
+            assert parts[0][0] == 0 and parts[-1][1] == kv[b]
+            for a, c in zip(parts, parts[1:]):
+                assert a[1] == c[0]                       # contiguous, no overlap
+            assert sorted(p[2] for p in parts) == list(range(parts[0][3]))
+            assert sum(1 for p in parts if p[2] == 0) == 1   # sink in exactly one chunk
+    # partial slots are disjoint per group
+    slots = set()
+    for row in u:
+        if row[8] > 1:
+            s = (row[10] + row[7])
+            assert s not in slots
+            slots.add(s)
+    assert len(slots) == info.num_decode_partials
+    lib.attn_plan_destroy(h)
+
+
+def test_decode_units_sorted_longest_first(lib):
+    kv = np.array([100, 5000, 17, 9000, 3000])
+    pages = (kv + 15) // 16
+    st, h, _ = plan(lib, [1] * 5, pages, kv - (pages - 1) * 16)
+    _, u, _ = units_of(lib, h)
+    lens = u[:, 6] - u[:, 5]
+    assert np.all(np.diff(lens) <= 0)
+    lib.attn_plan_destroy(h)
+
+
+@pytest.mark.parametrize("causal", [1, 0])
+def test_prefill_items_cover_rows_heads(lib, causal):
+    qo = np.array([300, 1, 2048, 129, 0, 5])
+    kv = np.array([300, 40, 4096, 1000, 7, 5])
+    pages = (kv + 15) // 16
+    last = kv - (pages - 1) * 16
+    st, h, _ = plan(lib, qo, pages, last, causal=causal)
+    assert st == OK
+    info, u, it = units_of(lib, h)
+    assert info.num_decode_requests == 1 and info.num_prefill_requests == 4
+    qo_indptr = np.concatenate([[0], np.cumsum(qo)])
+    seen = {}
+    for (row0, nrows, page_base, kv_len, pos0, g, head0, nh, ntiles, key_end, _, _) in it:
+        b = int(np.searchsorted(qo_indptr, row0, side="right") - 1)
+        assert kv_len == kv[b] and 1 <= nrows <= 128 and nh in (1, 2)
+        assert pos0 == kv[b] - qo[b] + (row0 - qo_indptr[b])
+        exp_end = min(kv[b], pos0 + nrows) if causal else kv[b]
+        assert key_end == exp_end and ntiles == -(-exp_end // 128)
+        for hh in range(head0, head0 + nh):
+            assert hh // 8 == g
+            for r in range(row0, row0 + nrows):
+                seen[(r, hh)] = seen.get((r, hh), 0) + 1
+    expected = {(r, hh) for b in range(len(qo)) if qo[b] > 1
+                for r in range(qo_indptr[b], qo_indptr[b + 1]) for hh in range(64)}
+    assert set(seen) == expected and all(v == 1 for v in seen.values())
+    pairs = sum((kv[b] - qo[b] + i + 1) if causal else kv[b]
+                for b in range(len(qo)) if qo[b] > 1 for i in range(qo[b]))
+    assert info.prefill_pairs == pairs
+    lib.attn_plan_destroy(h)
+
+
+def test_split_balances_small_batches(lib):
+    """Two long sequences on 152 SMs are split into many chunks."""
+    kv = np.array([32768, 32768])
+    pages = kv // 16
+    st, h, _ = plan(lib, [1, 1], pages, np.full(2, 16))
+    info, u, _ = units_of(lib, h)
+    assert info.num_decode_units >= 152
+    lib.attn_plan_destroy(h)
+
+
+@pytest.mark.parametrize("case", [
+    dict(qo=[2], kv_pages=[0], last=[0]),            # qo_len > kv_len
+    dict(qo=[1], kv_pages=[2], last=[0]),            # last_page_len out of range
+    dict(qo=[1], kv_pages=[2], last=[17]),
+    dict(qo=[1], kv_pages=[1], last=[4], Hq=6, Hkv=4),
+    dict(qo=[1], kv_pages=[1], last=[4], causal=2),
+])
+def test_plan_rejects_malformed(lib, case):
+    st, h, _ = plan(lib, **case)
+    assert st == INVALID
+
+
+@pytest.mark.parametrize("case", [dict(D=96), dict(P=8), dict(D=256)])
+def test_plan_rejects_unsupported(lib, case):
+    st, h, _ = plan(lib, [1], [1], [4], **case)
+    assert st == UNSUPPORTED
+
+
+def test_plan_null_and_negative_indptr(lib):
+    handle = ctypes.c_void_p()
+    ws = ctypes.c_size_t()
+    assert lib.attn_plan(None, None, None, None, 1, 8, 2, 64, 16, 1, 0.125, 10, 152,
+                         ctypes.byref(handle), ctypes.byref(ws)) == INVALID
+    st, h, _ = plan(lib, [3, -2], [1, 1], [4, 4])
+    assert st == INVALID
+
+
+def test_empty_batch_plan(lib):
+    st, h, ws = plan(lib, [], [], [])
+    assert st == OK
+    info, u, it = units_of(lib, h)
+    assert info.num_decode_units == 0 and info.num_prefill_items == 0
+    lib.attn_plan_destroy(h)
+
+
+def test_launch_without_workspace_is_rejected(lib):
+    st, h, _ = plan(lib, [1], [1], [4])
+    dummy = ctypes.c_void_p(0x10000)
+    assert lib.attn_decode(h, dummy, dummy, None, dummy, None, None) == 5   # not bound
+    assert lib.attn_plan_bind_workspace(h, ctypes.c_void_p(0x10001), 1 << 20, None) == INVALID
+    assert lib.attn_plan_bind_workspace(h, ctypes.c_void_p(0x10000), 1, None) == 3
+    lib.attn_plan_destroy(h)
+
+
+def test_merge_states_argument_checks(lib):
+    p = ctypes.c_void_p(0x10000)
+    assert lib.attn_merge_states(p, p, p, p, p, None, 4, 2, 6, None) == INVALID   # D % 4
+    assert lib.attn_merge_states(p, p, p, p, p, None, -1, 2, 8, None) == INVALID
+    assert lib.attn_merge_states(None, None, None, None, None, None, 0, 2, 8, None) == OK

@@ -1,0 +1,163 @@
+"""GPU parity of attn_decode against the fp64 oracle, through the C ABI.
+
+Decode: one query token per request (qo_len = 1) against its whole paged KV
+sequence, with the per-head sink in the softmax denominator ("GPT-OSS on day
+0", section "Sink Attention").  Pool pages no request uses and the tail of
+each last page hold NaN, so any stray read would poison the output.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import check_close, decode_rows, make_plan, sample_pairs, syn, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def run_decode(batch, sinks="batch", num_sms=0, with_lse=True):
+    q, kv, pt, sk = to_device(batch)
+    if not isinstance(sinks, str):
+        sk = None if sinks is None else torch.as_tensor(sinks, dtype=torch.float32, device="cuda")
+    plan = make_plan(batch, pt, num_sms=num_sms)
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full((batch.total_rows, batch.num_qo_heads), float("nan"), device="cuda") if with_lse else None
+    plan.decode(q, kv, sk, out, lse)
+    torch.cuda.synchronize()
+    assert plan.device_error() == 0
+    return out, lse, plan
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_tiny_decode(seed):
+    batch = syn.tiny_decode(seed)
+    out, lse, _ = run_decode(batch)
+    ref_out, ref_lse = oracle.sink_attention(batch)
+    check_close(out, lse, ref_out, ref_lse, "tiny")
+
+
+@pytest.mark.parametrize("variant", ["null", "neg_inf", "huge"])
+def test_tiny_decode_sink_variants(variant):
+    batch = syn.tiny_decode(1)
+    if variant == "null":
+        sinks = None
+    elif variant == "neg_inf":
+        sinks = np.full(batch.num_qo_heads, -np.inf, dtype=np.float32)
+    else:
+        sinks = np.full(batch.num_qo_heads, 80.0, dtype=np.float32)
+    out, lse, _ = run_decode(batch, sinks=sinks)
+    ref_out, ref_lse = oracle.sink_attention(batch, sinks=sinks)
+    check_close(out, lse, ref_out, ref_lse, variant)
+
+
+def test_gptoss_decode_full():
+    batch = syn.gptoss_decode(0)
+    out, lse, plan = run_decode(batch)
+    assert plan.info()["num_decode_groups_split"] > 0
+    ref_out, ref_lse = oracle.sink_attention(batch)
+    check_close(out, lse, ref_out, ref_lse, "gpt-oss decode")
+
+
+def test_qwen_decode_full_sampled():
+    batch = syn.qwen_decode(0)
+    out, lse, _ = run_decode(batch)
+    rows, heads = sample_pairs(batch, decode_rows(batch), 384, seed=3)
+    ref_out, ref_lse = oracle.sink_attention(batch, rows=rows, heads=heads)
+    o = out[torch.from_numpy(rows).cuda(), torch.from_numpy(heads).long().cuda()]
+    l = lse[torch.from_numpy(rows).cuda(), torch.from_numpy(heads).long().cuda()]
+    check_close(o, l, ref_out, ref_lse, "qwen decode")
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,P", [
+    (8, 8, 64, 16),      # G = 1
+    (32, 2, 64, 32),     # G = 16
+    (64, 2, 64, 16),     # G = 32: two head slices per KV head
+    (24, 2, 128, 16),    # G = 12, D = 128
+    (16, 1, 128, 128),   # G = 16, P = 128
+    (12, 4, 64, 64),     # G = 3
+])
+def test_decode_shapes(Hq, Hkv, D, P):
+    kv = [1, 15, 16, 17, P, P + 1, 3 * P - 1, 700, 2500]
+    batch = syn.make_batch("shapes", [1] * len(kv), kv, Hq, Hkv, D, P, seed=Hq + D + P)
+    out, lse, _ = run_decode(batch)
+    ref_out, ref_lse = oracle.sink_attention(batch)
+    check_close(out, lse, ref_out, ref_lse, f"{Hq}/{Hkv}/{D}/{P}")
+
+
+@pytest.mark.parametrize("num_sms", [1, 7, 152, 1000])
+def test_split_choices_agree(num_sms):
+    """Different split-KV chunkings all match the oracle."""
+    batch = syn.make_batch("split", [1] * 6, [33, 4000, 9000, 129, 16384, 2], 16, 2, 64, 16, seed=5)
+    out, lse, plan = run_decode(batch, num_sms=num_sms)
+    ref_out, ref_lse = oracle.sink_attention(batch)
+    check_close(out, lse, ref_out, ref_lse, f"sms={num_sms}")
+
+
+def test_identical_keys():
+    """All keys equal: out = mean(V) * n / (n + exp(sink - s))."""
+    batch = syn.make_batch("ident", [1, 1], [300, 45], 8, 2, 64, 16, seed=9)
+    used = batch.kv_pool[:, 0] != syn.BF16_NAN
+    one_key = syn.bf16_bits(np.random.default_rng(0).standard_normal(64).astype(np.float32))
+    batch.kv_pool[:, 0][used] = np.broadcast_to(one_key, batch.kv_pool[:, 0].shape)[used]
+    out, lse, _ = run_decode(batch)
+    ref_out, ref_lse = oracle.sink_attention(batch)
+    check_close(out, lse, ref_out, ref_lse, "identical keys")
+
+
+def test_page_permutation_gives_identical_bits():
+    batch = syn.make_batch("perm", [1] * 4, [700, 33, 1200, 16], 16, 2, 64, 16, pool_pages=200, seed=2)
+    out_a, lse_a, _ = run_decode(batch)
+    perm = np.random.default_rng(1).permutation(batch.num_pages)
+    pool = np.empty_like(batch.kv_pool)
+    pool[perm] = batch.kv_pool
+    batch.kv_pool = pool
+    batch.page_table = perm[batch.page_table].astype(np.int32)
+    out_b, lse_b, _ = run_decode(batch)
+    assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
+    assert torch.equal(lse_a, lse_b)
+
+
+def test_run_to_run_bitwise_deterministic():
+    batch = syn.gptoss_decode(1, batch=16)
+    q, kv, pt, sk = to_device(batch)
+    plan = make_plan(batch, pt)
+    outs = []
+    for _ in range(3):
+        out = torch.empty_like(q)
+        lse = torch.empty(batch.total_rows, batch.num_qo_heads, device="cuda")
+        plan.decode(q, kv, sk, out, lse)
+        outs.append((out.view(torch.int16).clone(), lse.clone()))
+    torch.cuda.synchronize()
+    for o, l in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
+
+
+def test_decode_leaves_prefill_rows_untouched():
+    batch = syn.make_batch("mixed_small", [5, 1, 3, 1], [40, 77, 3, 1], 8, 2, 64, 16, seed=4)
+    out, lse, _ = run_decode(batch)
+    ref_out, ref_lse = oracle.sink_attention(batch)
+    rows = decode_rows(batch)
+    check_close(out[rows], lse[rows], ref_out[rows], ref_lse[rows], "decode rows")
+    other = [r for r in range(batch.total_rows) if r not in rows]
+    assert torch.isnan(out[other].float()).all() and torch.isnan(lse[other]).all()
+
+
+def test_lse_optional():
+    batch = syn.tiny_decode(2)
+    out, _, _ = run_decode(batch, with_lse=False)
+    ref_out, _ = oracle.sink_attention(batch)
+    check_close(out, None, ref_out, None, "no lse")
+
+
+def test_bad_page_id_is_flagged_not_faulted():
+    """A page id outside the pool is caught by the kernel's own bounds check:
+    the load is skipped and the device error word reports it."""
+    batch = syn.tiny_decode(0)
+    q, kv, pt, sk = to_device(batch)
+    pt[3] = batch.num_pages + 5
+    plan = make_plan(batch, pt)
+    out = torch.empty_like(q)
+    plan.decode(q, kv, sk, out, None)
+    assert plan.device_error() & 1
+    assert plan.device_error() == 0     # cleared by the read
