@@ -1,0 +1,137 @@
+"""GPU parity of attn_prefill (tcgen05 tensor-core kernel) against the fp64
+oracle, through the C ABI.
+
+Prefill: qo_len > 1 query tokens per request, causal with bottom-right
+alignment when a cached prefix precedes them, sink in the denominator ("GPT-OSS
+on day 0", section "Sink Attention"; request model of "Disaggregated prefill
+and decode", section "Prefill vs decode performance").
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import check_close, make_plan, prefill_rows, sample_pairs, syn, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def run_prefill(batch, sinks="batch", with_lse=True):
+    q, kv, pt, sk = to_device(batch)
+    if not isinstance(sinks, str):
+        sk = None if sinks is None else torch.as_tensor(sinks, dtype=torch.float32, device="cuda")
+    plan = make_plan(batch, pt)
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full((batch.total_rows, batch.num_qo_heads), float("nan"), device="cuda") if with_lse else None
+    plan.prefill(q, kv, sk, out, lse)
+    torch.cuda.synchronize()
+    assert plan.device_error() == 0
+    return out, lse, plan
+
+
+def _check_rows(batch, out, lse, sinks="batch", what=""):
+    ref_out, ref_lse = oracle.sink_attention(batch, sinks=sinks)
+    rows = prefill_rows(batch)
+    return check_close(out[rows], None if lse is None else lse[rows], ref_out[rows],
+                       None if lse is None else ref_lse[rows], what)
+
+
+@pytest.mark.parametrize("lens", [[200, 77], [128, 256, 2, 129], [300], [1000, 513]])
+def test_prefill_causal_small(lens):
+    batch = syn.make_batch("pf", lens, lens, 8, 2, 64, 16, seed=len(lens) + lens[0])
+    out, lse, _ = run_prefill(batch)
+    _check_rows(batch, out, lse, what=f"causal {lens}")
+
+
+def test_prefill_with_cached_prefix():
+    """qo_len < kv_len: rows are aligned to the end of the sequence."""
+    qo = [64, 200, 130, 7]
+    kv = [64, 2248, 4226, 100]
+    batch = syn.make_batch("prefix", qo, kv, 8, 2, 64, 16, seed=3)
+    out, lse, _ = run_prefill(batch)
+    _check_rows(batch, out, lse, what="prefix")
+
+
+def test_prefill_non_causal():
+    batch = syn.make_batch("nc", [100, 260], [300, 260], 8, 2, 64, 16, causal=False, seed=4)
+    out, lse, _ = run_prefill(batch)
+    _check_rows(batch, out, lse, what="non-causal")
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,P", [
+    (8, 8, 64, 16),     # G = 1: one head per CTA
+    (12, 4, 64, 32),    # G = 3: a pair and a single
+    (16, 2, 128, 64),   # D = 128
+    (8, 2, 64, 128),    # one page per KV tile
+    (4, 1, 128, 16),
+])
+def test_prefill_shapes(Hq, Hkv, D, P):
+    qo = [300, 129, 64]
+    kv = [300, 500, 64]
+    batch = syn.make_batch("shapes", qo, kv, Hq, Hkv, D, P, seed=Hq * D + P)
+    out, lse, _ = run_prefill(batch)
+    _check_rows(batch, out, lse, what=f"{Hq}/{Hkv}/{D}/{P}")
+
+
+@pytest.mark.parametrize("variant", ["null", "huge"])
+def test_prefill_sink_variants(variant):
+    batch = syn.make_batch("sinkvar", [150, 40], [150, 90], 8, 2, 64, 16, seed=6)
+    sinks = None if variant == "null" else np.full(8, 80.0, dtype=np.float32)
+    out, lse, _ = run_prefill(batch, sinks=sinks)
+    _check_rows(batch, out, lse, sinks=sinks, what=variant)
+
+
+def test_prefill_large_scores_rescale():
+    """Scaled-up queries make the running max jump across tiles, exercising
+    the lazy O rescale."""
+    batch = syn.make_batch("scale", [700], [700], 4, 1, 64, 16, seed=7)
+    q = syn.bf16_to_float(batch.q) * 6.0
+    batch.q = syn.bf16_bits(q)
+    out, lse, _ = run_prefill(batch)
+    _check_rows(batch, out, lse, what="large scores")
+
+
+def test_gptoss_prefill_full_sampled():
+    batch = syn.gptoss_prefill(0)
+    out, lse, plan = run_prefill(batch)
+    rows, heads = sample_pairs(batch, prefill_rows(batch), 512, seed=1)
+    ref_out, ref_lse = oracle.sink_attention(batch, rows=rows, heads=heads)
+    ri = torch.from_numpy(rows).cuda()
+    hi = torch.from_numpy(heads).long().cuda()
+    check_close(out[ri, hi], lse[ri, hi], ref_out, ref_lse, "gpt-oss prefill")
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+
+
+def test_mixed_batch_full_sampled():
+    """One plan, prefill then decode on the same stream."""
+    batch = syn.mixed(0)
+    q, kv, pt, sk = to_device(batch)
+    plan = make_plan(batch, pt)
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full((batch.total_rows, batch.num_qo_heads), float("nan"), device="cuda")
+    plan.prefill(q, kv, sk, out, lse)
+    plan.decode(q, kv, sk, out, lse)
+    torch.cuda.synchronize()
+    assert plan.device_error() == 0
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+    all_rows = list(range(batch.total_rows))
+    rows, heads = sample_pairs(batch, all_rows, 768, seed=2)
+    ref_out, ref_lse = oracle.sink_attention(batch, rows=rows, heads=heads)
+    ri = torch.from_numpy(rows).cuda()
+    hi = torch.from_numpy(heads).long().cuda()
+    check_close(out[ri, hi], lse[ri, hi], ref_out, ref_lse, "mixed")
+
+
+def test_prefill_bitwise_deterministic():
+    batch = syn.make_batch("det", [400, 130], [400, 300], 8, 2, 64, 16, seed=8)
+    q, kv, pt, sk = to_device(batch)
+    plan = make_plan(batch, pt)
+    res = []
+    for _ in range(3):
+        out = torch.empty_like(q)
+        lse = torch.empty(batch.total_rows, batch.num_qo_heads, device="cuda")
+        plan.prefill(q, kv, sk, out, lse)
+        res.append((out.view(torch.int16).clone(), lse.clone()))
+    torch.cuda.synchronize()
+    for o, l in res[1:]:
+        assert torch.equal(o, res[0][0]) and torch.equal(l, res[0][1])
