@@ -44,7 +44,7 @@ struct DecodeCfg {
     static constexpr int kPipeBytes = kWarps * kStages * kStageBytes;
     static constexpr int kPageBytes = (kDecodeMaxChunkPages * 4 + 15) / 16 * 16;
     static constexpr int kBarBytes = kWarps * kStages * 8;
-    static constexpr int kStateBytes = kWarps * 32 * 4 + 16;  // per-warp m, l + flag
+    static constexpr int kStateBytes = kWarps * 48 * 4 + 16;  // per-warp m, l, le + flag
     static constexpr int kSmem = 1024 + kPipeBytes + kPageBytes + kBarBytes + kStateBytes;
     static constexpr int kRowStride = D + 8;                  // floats, combine buffers
     static_assert(kBlockTokens * kRowStride * 4 <= kStages * kStageBytes, "combine fits");
@@ -87,7 +87,7 @@ decode_sink_attn_kernel(const __grid_constant__ CUtensorMap kv_map, const Decode
     int32_t* pages_s = reinterpret_cast<int32_t*>(smem + C::kPipeBytes);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kPipeBytes + C::kPageBytes);
     float* ml_s = reinterpret_cast<float*>(smem + C::kPipeBytes + C::kPageBytes + C::kBarBytes);
-    int* flag_s = reinterpret_cast<int*>(ml_s + C::kWarps * 32);
+    int* flag_s = reinterpret_cast<int*>(ml_s + C::kWarps * 48);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gq = lane >> 2, tq = lane & 3;
@@ -153,16 +153,18 @@ decode_sink_attn_kernel(const __grid_constant__ CUtensorMap kv_map, const Decode
     }
 
     // Online-softmax state (log2 domain).  l is a per-thread partial sum over
-    // this thread's columns; the sink's 1 is counted once, on column lane 0.
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    // this thread's columns of the bf16-rounded P that the PV MMA consumes (it
+    // normalises O); e is the same sum of the unrounded P (it gives lse).  The
+    // sink's 1 is counted once, on column lane 0.
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, e0 = 0.f, e1 = 0.f;
     if (warp == 0 && u.chunk == 0 && a.sinks != nullptr) {
         if (gq < u.n_heads) {
             m0 = a.sinks[u.head0 + gq] * kLog2e;
-            l0 = tq == 0 ? 1.f : 0.f;
+            l0 = e0 = tq == 0 ? 1.f : 0.f;
         }
         if (kTwoRows && gq + 8 < u.n_heads) {
             m1 = a.sinks[u.head0 + gq + 8] * kLog2e;
-            l1 = tq == 0 ? 1.f : 0.f;
+            l1 = e1 = tq == 0 ? 1.f : 0.f;
         }
     }
     float o[D / 8][4];
@@ -215,21 +217,21 @@ decode_sink_attn_kernel(const __grid_constant__ CUtensorMap kv_map, const Decode
                 x[nt][e] = tok < valid ? sc[nt][e] * a.scale_log2 : -INFINITY;
             }
         float p[2][4];
+        float alpha0, alpha1 = 1.f;
         {
             float mx = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
             const float mn = fmaxf(m0, mx);
             const float base = mn == -INFINITY ? 0.f : mn;
-            const float alpha = ptx::ex2(m0 - base);
+            alpha0 = ptx::ex2(m0 - base);
             p[0][0] = ptx::ex2(x[0][0] - base);
             p[0][1] = ptx::ex2(x[0][1] - base);
             p[1][0] = ptx::ex2(x[1][0] - base);
             p[1][1] = ptx::ex2(x[1][1] - base);
-            l0 = l0 * alpha + (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
             m0 = mn;
 #pragma unroll
-            for (int j = 0; j < D / 8; ++j) { o[j][0] *= alpha; o[j][1] *= alpha; }
+            for (int j = 0; j < D / 8; ++j) { o[j][0] *= alpha0; o[j][1] *= alpha0; }
         }
         if (kTwoRows) {
             float mx = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
@@ -237,15 +239,14 @@ decode_sink_attn_kernel(const __grid_constant__ CUtensorMap kv_map, const Decode
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
             const float mn = fmaxf(m1, mx);
             const float base = mn == -INFINITY ? 0.f : mn;
-            const float alpha = ptx::ex2(m1 - base);
+            alpha1 = ptx::ex2(m1 - base);
             p[0][2] = ptx::ex2(x[0][2] - base);
             p[0][3] = ptx::ex2(x[0][3] - base);
             p[1][2] = ptx::ex2(x[1][2] - base);
             p[1][3] = ptx::ex2(x[1][3] - base);
-            l1 = l1 * alpha + (p[0][2] + p[0][3]) + (p[1][2] + p[1][3]);
             m1 = mn;
 #pragma unroll
-            for (int j = 0; j < D / 8; ++j) { o[j][2] *= alpha; o[j][3] *= alpha; }
+            for (int j = 0; j < D / 8; ++j) { o[j][2] *= alpha1; o[j][3] *= alpha1; }
         } else {
             p[0][2] = p[0][3] = p[1][2] = p[1][3] = 0.f;
         }
@@ -254,6 +255,17 @@ decode_sink_attn_kernel(const __grid_constant__ CUtensorMap kv_map, const Decode
         pa[1] = ptx::pack_bf16x2(p[0][2], p[0][3]);
         pa[2] = ptx::pack_bf16x2(p[1][0], p[1][1]);
         pa[3] = ptx::pack_bf16x2(p[1][2], p[1][3]);
+        {
+            // Row sums of the same bf16-rounded P that the PV MMA uses.
+            const float2 a0 = ptx::unpack_bf16x2(pa[0]), a2 = ptx::unpack_bf16x2(pa[2]);
+            l0 = l0 * alpha0 + (a0.x + a0.y) + (a2.x + a2.y);
+            e0 = e0 * alpha0 + (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
+            if (kTwoRows) {
+                const float2 a1 = ptx::unpack_bf16x2(pa[1]), a3 = ptx::unpack_bf16x2(pa[3]);
+                l1 = l1 * alpha1 + (a1.x + a1.y) + (a3.x + a3.y);
+                e1 = e1 * alpha1 + (p[0][2] + p[0][3]) + (p[1][2] + p[1][3]);
+            }
+        }
 
         // O[head][dim] += P V (V read transposed by ldmatrix.trans).
 #pragma unroll
@@ -286,6 +298,10 @@ decode_sink_attn_kernel(const __grid_constant__ CUtensorMap kv_map, const Decode
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    e0 += __shfl_xor_sync(0xffffffffu, e0, 1);
+    e0 += __shfl_xor_sync(0xffffffffu, e0, 2);
+    e1 += __shfl_xor_sync(0xffffffffu, e1, 1);
+    e1 += __shfl_xor_sync(0xffffffffu, e1, 2);
     float* cs = reinterpret_cast<float*>(pipe + warp * C::kStages * C::kStageBytes);
 #pragma unroll
     for (int j = 0; j < D / 8; ++j) {
@@ -294,10 +310,13 @@ decode_sink_attn_kernel(const __grid_constant__ CUtensorMap kv_map, const Decode
         *reinterpret_cast<float2*>(&cs[(gq + 8) * C::kRowStride + d]) = make_float2(o[j][2], o[j][3]);
     }
     if (tq == 0) {
-        ml_s[warp * 32 + gq] = m0;
-        ml_s[warp * 32 + 16 + gq] = l0;
-        ml_s[warp * 32 + gq + 8] = kTwoRows ? m1 : -INFINITY;
-        ml_s[warp * 32 + 16 + gq + 8] = kTwoRows ? l1 : 0.f;
+        float* st = ml_s + warp * 48;   // [m | l | e] x 16 rows
+        st[gq] = m0;
+        st[16 + gq] = l0;
+        st[32 + gq] = e0;
+        st[gq + 8] = kTwoRows ? m1 : -INFINITY;
+        st[16 + gq + 8] = kTwoRows ? l1 : 0.f;
+        st[32 + gq + 8] = kTwoRows ? e1 : 0.f;
     }
     __syncthreads();
 
@@ -307,20 +326,21 @@ decode_sink_attn_kernel(const __grid_constant__ CUtensorMap kv_map, const Decode
         const int r = idx / (D / 4), d = (idx % (D / 4)) * 4;
         float ms = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < C::kWarps; ++w) ms = fmaxf(ms, ml_s[w * 32 + r]);
-        float L = 0.f;
+        for (int w = 0; w < C::kWarps; ++w) ms = fmaxf(ms, ml_s[w * 48 + r]);
+        float L = 0.f, E = 0.f;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int w = 0; w < C::kWarps; ++w) {
-            const float mw = ml_s[w * 32 + r];
+            const float mw = ml_s[w * 48 + r];
             const float f = (mw == -INFINITY) ? 0.f : ptx::ex2(mw - ms);
-            L += f * ml_s[w * 32 + 16 + r];
+            L += f * ml_s[w * 48 + 16 + r];
+            E += f * ml_s[w * 48 + 32 + r];
             const float4 ow = *reinterpret_cast<const float4*>(
                 reinterpret_cast<const float*>(pipe + w * C::kStages * C::kStageBytes) + r * C::kRowStride + d);
             acc.x += f * ow.x; acc.y += f * ow.y; acc.z += f * ow.z; acc.w += f * ow.w;
         }
         const float inv = L > 0.f ? 1.f / L : 0.f;
-        const float lse2 = L > 0.f ? ms + log2f(L) : -INFINITY;
+        const float lse2 = E > 0.f ? ms + log2f(E) : -INFINITY;
         if (u.n_chunks == 1) {
             store_bf16x4(a.out + ((size_t)u.q_row * a.Hq + u.head0 + r) * D + d, acc.x * inv,
                          acc.y * inv, acc.z * inv, acc.w * inv);

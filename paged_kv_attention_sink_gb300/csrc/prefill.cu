@@ -284,10 +284,12 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
             const uint32_t t_s = tmem + ((uint32_t)(quad * 32) << 16) + i * 128;
             const uint32_t t_o = tmem + ((uint32_t)(quad * 32) << 16) + 256 + i * D;
             const float sl2 = a.scale_log2;
-            float m_use = -INFINITY, l = 0.f;
+            // l: row sum of the bf16-rounded P that the PV MMA consumes (it
+            // normalises O); le: the same sum of the unrounded P (it gives lse).
+            float m_use = -INFINITY, l = 0.f, le = 0.f;
             if (a.sinks != nullptr) {
                 m_use = a.sinks[head] * kLog2e;
-                l = 1.f;
+                l = le = 1.f;
             }
             // Last key this row may see, and the first tile that needs a mask
             // (every earlier tile is fully visible to every row of the tile).
@@ -323,6 +325,7 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                 if (m_new > m_use + kRescaleThreshold || (m_use == -INFINITY && m_new != -INFINITY)) {
                     alpha = ptx::ex2(m_use - m_new);
                     l *= alpha;
+                    le *= alpha;
                     m_use = m_new;
                     rescale = j > 0;
                 }
@@ -339,7 +342,7 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                     }
                 }
                 const float neg_m = m_use == -INFINITY ? 0.f : -m_use;
-                float ls0 = 0.f, ls1 = 0.f;
+                float ls0 = 0.f, ls1 = 0.f, le0 = 0.f, le1 = 0.f;
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     uint32_t pk[32];
@@ -347,13 +350,17 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                     for (int e = 0; e < 32; ++e) {
                         const float p0 = ptx::ex2(fmaf(s[c * 64 + 2 * e], sl2, neg_m));
                         const float p1 = ptx::ex2(fmaf(s[c * 64 + 2 * e + 1], sl2, neg_m));
-                        ls0 += p0;
-                        ls1 += p1;
                         pk[e] = ptx::pack_bf16x2(p0, p1);
+                        const float2 pr = ptx::unpack_bf16x2(pk[e]);
+                        ls0 += pr.x;
+                        ls1 += pr.y;
+                        le0 += p0;
+                        le1 += p1;
                     }
                     ptx::tmem_st32(t_s + c * 32, pk);
                 }
                 l += ls0 + ls1;
+                le += le0 + le1;
                 ptx::tc_wait_st();
                 ptx::tc_fence_before();
                 __syncwarp();
@@ -386,7 +393,7 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                 }
                 if (store && a.lse)
                     a.lse[(size_t)(it.q_row0 + r) * a.Hq + head] =
-                        l > 0.f ? (m_use + log2f(l)) * kLn2 : -INFINITY;
+                        le > 0.f ? (m_use + log2f(le)) * kLn2 : -INFINITY;
             }
         }
     }
