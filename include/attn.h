@@ -181,6 +181,33 @@ ATTN_API attn_status attn_merge_states(const void* va, const float* lsea, const 
                               const float* lseb, void* vout, float* lseout, int32_t n_tokens,
                               int32_t n_heads, int32_t head_dim, void* stream);
 
+/*
+ * attn_decode_noalloc -- attn_decode for callers that cannot allocate device
+ * memory when they run attention (for example an engine that replays a
+ * captured CUDA graph, or one that reserves its memory budget up front and
+ * forbids cudaMalloc, and with it cudaMalloc's implicit device sync, while it
+ * serves).  The paper has no counterpart: this is an interface addition.
+ *
+ * Same arguments and results as attn_decode, but the plan needs no bound
+ * workspace: the work list, split-KV partial states, merge counters and error
+ * word live in a static 16 MiB device array inside the library, which every
+ * GPU that loads the library holds until the process exits.  Plans whose
+ * workspace_bytes exceed 16 MiB are rejected with ATTN_ERR_WORKSPACE_TOO_SMALL.
+ * It allocates nothing (no cudaMalloc / cudaFree): each call uploads the work
+ * list with cudaMemcpyAsync and zeroes the counters with cudaMemsetAsync on
+ * `stream`, then launches the decode kernel.
+ *
+ * The first call on a device resolves the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  All calls share the one array and it keeps the
+ * last call's contents, so calls that overlap on the GPU (other streams, other
+ * host threads) race: serialise them.  Device-side error bits of this path
+ * are not reported (attn_plan_device_error reads the bound workspace only);
+ * bad page ids are still skipped rather than read.
+ */
+ATTN_API attn_status attn_decode_noalloc(attn_plan_t plan, const void* q, const void* kv_cache,
+                                         const float* sinks, void* out, float* lse, void* stream);
+
 /* Copy the plan's summary into *info (host only). */
 ATTN_API attn_status attn_plan_get_info(attn_plan_t plan, attn_plan_info* info);
 

@@ -53,6 +53,7 @@ def _declare(lib):
         "attn_plan_bind_workspace": (st, [p, p, ctypes.c_size_t, p]),
         "attn_decode": (st, [p, p, p, p, p, p, p]),
         "attn_prefill": (st, [p, p, p, p, p, p, p]),
+        "attn_decode_noalloc": (st, [p, p, p, p, p, p, p]),
         "attn_merge_states": (st, [p, p, p, p, p, p, i32, i32, i32, p]),
         "attn_plan_get_info": (st, [p, p]),
         "attn_plan_get_decode_units": (st, [p, p, i64]),

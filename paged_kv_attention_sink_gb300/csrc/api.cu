@@ -153,3 +153,9 @@ extern "C" attn_status attn_plan_device_error(attn_plan_t plan, int32_t* code, v
     *code = v;
     return v != 0 ? ATTN_ERR_DEVICE : ATTN_OK;
 }
+
+namespace attn {
+bool encode_decode_kv_map(void* map, const void* kv_cache, const attn_plan_s* plan) {
+    return make_kv_map(map, kv_cache, plan, kBlockTokens);
+}
+}  // namespace attn

@@ -441,3 +441,38 @@ attn_status launch_decode(attn_plan_s* plan, const void* q, const void* kv_map, 
 }
 
 }  // namespace attn
+
+namespace attn {
+
+attn_status launch_decode_scratch(attn_plan_s* plan, unsigned char* scratch, const void* q,
+                                  const void* kv_map, const float* sinks, void* out, float* lse,
+                                  cudaStream_t stream) {
+    if (plan->units.empty()) return ATTN_OK;
+    DecodeArgs a;
+    a.units = reinterpret_cast<const DecodeUnit*>(scratch + plan->layout.units);
+    a.page_table = plan->page_table;
+    a.q = static_cast<const __nv_bfloat16*>(q);
+    a.out = static_cast<__nv_bfloat16*>(out);
+    a.lse = lse;
+    a.sinks = sinks;
+    a.part_o = reinterpret_cast<float*>(scratch + plan->layout.part_o);
+    a.part_lse = reinterpret_cast<float*>(scratch + plan->layout.part_lse);
+    a.counters = reinterpret_cast<int32_t*>(scratch + plan->layout.counters);
+    a.err = reinterpret_cast<int32_t*>(scratch + plan->layout.err);
+    a.Hq = plan->Hq;
+    a.Hkv = plan->Hkv;
+    a.P = plan->P;
+    a.num_pages = plan->num_pages;
+    a.scale_log2 = plan->sm_scale * kLog2e;
+    const CUtensorMap& map = *static_cast<const CUtensorMap*>(kv_map);
+    const bool two_rows = plan->Hq / plan->Hkv > 8;
+    const int n = (int)plan->units.size();
+    cudaError_t e;
+    if (plan->D == 64)
+        e = two_rows ? launch<64, true>(map, a, n, stream) : launch<64, false>(map, a, n, stream);
+    else
+        e = two_rows ? launch<128, true>(map, a, n, stream) : launch<128, false>(map, a, n, stream);
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace attn

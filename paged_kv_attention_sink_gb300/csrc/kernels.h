@@ -17,3 +17,18 @@ attn_status launch_merge_states(const void* va, const float* lsea, const void* v
                                 int head_dim, cudaStream_t stream);
 
 }  // namespace attn
+
+namespace attn {
+
+// Same decode launch as launch_decode, but with the plan's device work list,
+// partial states, merge counters and error word taken from `scratch` (laid
+// out as the plan's workspace) instead of the bound workspace.
+attn_status launch_decode_scratch(attn_plan_s* plan, unsigned char* scratch, const void* q,
+                                  const void* kv_map, const float* sinks, void* out, float* lse,
+                                  cudaStream_t stream);
+
+// Build the decode kernel's KV tensor map for `kv_cache` into `map` (128 bytes,
+// 64-byte aligned).  Returns false if the driver rejects it.
+bool encode_decode_kv_map(void* map, const void* kv_cache, const attn_plan_s* plan);
+
+}  // namespace attn
