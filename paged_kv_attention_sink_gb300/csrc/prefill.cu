@@ -5,21 +5,32 @@
 // online with max subtraction, the running max initialised to the sink (scale
 // 1).  Prefill is compute-bound ("Disaggregated prefill and decode", section
 // "Prefill vs decode performance"), so QK^T and PV run as tcgen05.mma with
-// fp32 accumulators in tensor memory:
+// fp32 accumulators in tensor memory.
 //
-//  * one CTA = 128 query rows of one request x two query heads of one GQA
-//    group; both heads share every K/V tile (each tile feeds four MMAs);
-//  * warp 0 (one lane) streams K/V tiles of 128 keys with TMA, one box per
-//    HND page, 128-byte swizzled, into a 3-stage ring; rows past the end of
-//    the sequence are zeroed in V before the MMA may read them;
-//  * warp 1 (one lane) issues the MMAs: S_h = Q_h K^T (both operands K-major
-//    in shared memory) and O_h += P_h V (P read straight from tensor memory,
-//    V as an MN-major shared-memory operand);
-//  * warps 4-7 and 8-11 run the softmax of head 0 and head 1: one thread per
-//    row (= TMEM lane) loads its 128 scores, applies the causal / length mask,
-//    updates the running max lazily (O is rescaled only when the max grew by
-//    more than 2^8), writes P as bf16 back over S in tensor memory, and at
-//    the end normalises O and stores out and lse.
+// Work item = 128 query rows of one request x two query heads of one GQA group
+// (both heads share every K/V tile).  The grid is persistent: one CTA per SM
+// walks the planner's longest-first item list with a stride of gridDim.x, so
+// the next item's Q and K/V loads and QK^T overlap the current item's last
+// softmax and epilogue.  Roles (12 warps = 3 warpgroups):
+//
+//  * warp 0: TMA producer.  Q tiles (double-buffered at D = 64), K and V rings
+//    of 128-key tiles, one box per HND page issued by its own lane (the
+//    boxes of a tile leave in one warp instruction), 128-byte swizzled.  V rows past
+//    the end of the sequence are zeroed before the MMA may read them.
+//  * warps 1 and 2, one lane each: tcgen05.mma issuers, one per head slot
+//    (neither head's MMAs queue behind the other's softmax).  S_h = Q_h K^T (both operands
+//    K-major in shared memory); O_h += P_h V with P read from tensor memory
+//    and V an MN-major shared-memory operand.  At D = 64, P has its own TMEM
+//    columns, so S_h of tile j+1 is computed while the softmax of tile j runs.
+//  * warps 4-7 / 8-11: softmax of head 0 / head 1, one thread per query row
+//    (= TMEM lane).  Causal / length mask on diagonal and ragged tiles only;
+//    the running max is raised lazily (O is rescaled in TMEM only when the max
+//    grew by more than 2^8); P is rounded to bf16 and O is normalised by the
+//    row sum of that rounded P, while lse uses the unrounded sum.
+//  * warp 3 idle (it keeps warpgroup 0 whole for setmaxnreg).
+//
+// TMEM (512 columns): S0 S1 (128 each), O0 O1 (D each), and at D = 64 P0 P1
+// (64 each); at D = 128 P aliases the first half of S.
 // Every wait is bounded; a timeout sets the device error word.
 #include <cuda.h>
 
@@ -36,7 +47,7 @@ constexpr float kRescaleThreshold = 8.0f;   // log2 units: P stays <= 2^8 betwee
 
 template <int D>
 struct PrefillCfg {
-    static constexpr int kThreads = 384;                 // 3 warpgroups
+    static constexpr int kThreads = 384;
     // Register split (setmaxnreg): the launch gives every thread kRegsLaunch;
     // warpgroup 0 (producer, MMA) drops to kRegsCtrl and the two softmax
     // warpgroups grow to kRegsSoftmax.  128 * kRegsCtrl + 256 * kRegsSoftmax
@@ -45,21 +56,27 @@ struct PrefillCfg {
     static constexpr int kRegsCtrl = 56;
     static constexpr int kRegsSoftmax = 224;
     static_assert(128 * kRegsCtrl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split");
+
+    static constexpr bool kSeparateP = (D == 64);
+    static constexpr int kQBufs = (D == 64) ? 2 : 1;
     static constexpr int kStagesK = (D == 64) ? 3 : 2;
     static constexpr int kStagesV = (D == 64) ? 3 : 2;
     static constexpr int kAtom = 128 * 128;              // 128 rows x 64 bf16, swizzled
     static constexpr int kTile = kAtom * (D / 64);       // Q, K or V tile of 128 rows
     static constexpr int kOffQ = 0;
-    static constexpr int kOffK = 2 * kTile;
+    static constexpr int kOffK = kQBufs * 2 * kTile;
     static constexpr int kOffV = kOffK + kStagesK * kTile;
     static constexpr int kOffBar = kOffV + kStagesV * kTile;
-    static constexpr int kNumBars = 1 + 2 * kStagesK + 2 * kStagesV + 6 + 2;
+    static constexpr int kNumBars = 2 * kQBufs + 2 * kStagesK + 2 * kStagesV + 8 + 2;
     static constexpr int kSmem = 1024 + kOffBar + kNumBars * 8 + 16;
-    static constexpr uint32_t kTmemCols = 512;           // S0 S1 (128 each), O0 O1 (D each)
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kColS = 0, kColO = 256, kColP = kSeparateP ? 384 : 0;
+    static constexpr uint32_t kStrideP = kSeparateP ? 64 : 128;
 };
 
 struct PrefillArgs {
     const PrefillItem* items;
+    int32_t n_items;
     const int32_t* page_table;
     __nv_bfloat16* out;
     float* lse;
@@ -70,8 +87,14 @@ struct PrefillArgs {
 };
 
 struct Bars {
-    uint32_t q_full, k_full, k_empty, v_full, v_empty, s_full, p_full, o_done, v_aux, drain;
+    uint32_t q_full, q_empty, k_full, k_empty, v_full, v_empty, s_full, s_free, p_full, o_done,
+        v_aux, drain;
 };
+
+// Warp-uniform bounded wait.
+__device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity));
+}
 
 template <int D>
 __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
@@ -88,38 +111,43 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
 
     Bars B;
     B.q_full = ptx::smem_u32(bar_mem);
-    B.k_full = B.q_full + 8;
+    B.q_empty = B.q_full + 8 * C::kQBufs;
+    B.k_full = B.q_empty + 8 * C::kQBufs;
     B.k_empty = B.k_full + 8 * C::kStagesK;
     B.v_full = B.k_empty + 8 * C::kStagesK;
     B.v_empty = B.v_full + 8 * C::kStagesV;
     B.s_full = B.v_empty + 8 * C::kStagesV;
-    B.p_full = B.s_full + 16;
+    B.s_free = B.s_full + 16;
+    B.p_full = B.s_free + 16;
     B.o_done = B.p_full + 16;
     B.v_aux = B.o_done + 16;
     B.drain = B.v_aux + 8;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const PrefillItem it = a.items[blockIdx.x];
-    const int n_tiles = it.n_kv_tiles;
-    const int nh = it.n_heads;
 
     if (tid == 0) {
-        ptx::mbar_init(B.q_full, 1);
+        // The "empty" barriers and `drain` take one arrival from each of the
+        // two MMA threads (head slots 0 and 1).
+        for (int b = 0; b < C::kQBufs; ++b) {
+            ptx::mbar_init(B.q_full + 8 * b, 1);
+            ptx::mbar_init(B.q_empty + 8 * b, 2);
+        }
         for (int s = 0; s < C::kStagesK; ++s) {
             ptx::mbar_init(B.k_full + 8 * s, 1);
-            ptx::mbar_init(B.k_empty + 8 * s, 1);
+            ptx::mbar_init(B.k_empty + 8 * s, 2);
         }
         for (int s = 0; s < C::kStagesV; ++s) {
             ptx::mbar_init(B.v_full + 8 * s, 1);
-            ptx::mbar_init(B.v_empty + 8 * s, 1);
+            ptx::mbar_init(B.v_empty + 8 * s, 2);
         }
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(B.s_full + 8 * i, 1);
+            ptx::mbar_init(B.s_free + 8 * i, 4);
             ptx::mbar_init(B.p_full + 8 * i, 4);
             ptx::mbar_init(B.o_done + 8 * i, 1);
         }
         ptx::mbar_init(B.v_aux, 1);
-        ptx::mbar_init(B.drain, 1);
+        ptx::mbar_init(B.drain, 2);
         *abort_flag = 0;
         ptx::prefetch_tmap(&q_map);
         ptx::prefetch_tmap(&kv_map);
@@ -142,148 +170,247 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
     if (warp < 4) ptx::setmaxnreg_dec<C::kRegsCtrl>();
 
     if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            ptx::mbar_arrive_expect_tx(B.q_full, nh * C::kTile);
-            for (int i = 0; i < nh; ++i)
-                for (int c = 0; c < D / 64; ++c)
-                    ptx::tma_load_3d(sbase + C::kOffQ + i * C::kTile + c * C::kAtom, &q_map, B.q_full,
-                                     c * 64, it.head0 + i, it.q_row0);
-        }
+        // ================================================================ producer
         const int P = a.P;
         const int pages_per_tile = kPrefillKeys / P;
         const int box_bytes = P * 128;               // P rows x 64 bf16
         const uint64_t policy = ptx::policy_evict_last();
-        int issued = 0;   // tiles whose loads were started
-        for (int j = 0; j < n_tiles; ++j) {
-            if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+        int jg = 0, n_item = 0, n_aux = 0;
+        int issued_k = 0, issued_v = 0;
+        bool ok = true;
+        // The producer walks this CTA's tiles (item, j) in order.  The page ids
+        // of the next tile are loaded (one per lane) while the current tile is
+        // issued, so the dependent global load never sits between two tiles.
+        auto n_load_of = [&](const PrefillItem& x, int j) {
+            return (min(kPrefillKeys, x.kv_len - j * kPrefillKeys) + P - 1) / P;
+        };
+        auto load_pages = [&](const PrefillItem& x, int j) {
+            return lane < n_load_of(x, j) ? a.page_table[x.page_base + j * pages_per_tile + lane] : -1;
+        };
+        int item = blockIdx.x, j = 0;
+        PrefillItem it = a.items[item];
+        int page = load_pages(it, 0);
+        while (item < a.n_items) {
+            if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
+            // Next tile of the walk and its page ids.
+            int item_n = item, j_n = j + 1;
+            PrefillItem it_n = it;
+            if (j_n == it.n_kv_tiles) {
+                item_n = item + gridDim.x;
+                j_n = 0;
+                if (item_n < a.n_items) it_n = a.items[item_n];
+            }
+            const int page_n = item_n < a.n_items ? load_pages(it_n, j_n) : -1;
+
+            if (j == 0) {
+                const int qb = n_item % C::kQBufs;
+                if (n_item >= C::kQBufs && !wait_all(B.q_empty + 8 * qb, ((n_item / C::kQBufs) - 1) & 1)) {
+                    fail(ATTN_DEVICE_ERR_TIMEOUT);
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    ptx::mbar_arrive_expect_tx(B.q_full + 8 * qb, it.n_heads * C::kTile);
+                    for (int i = 0; i < it.n_heads; ++i)
+                        for (int c = 0; c < D / 64; ++c)
+                            ptx::tma_load_3d(sbase + C::kOffQ + (qb * 2 + i) * C::kTile + c * C::kAtom, &q_map,
+                                             B.q_full + 8 * qb, c * 64, it.head0 + i, it.q_row0);
+                }
+            }
             const int valid = min(kPrefillKeys, it.kv_len - j * kPrefillKeys);
             const int n_load = (valid + P - 1) / P;
-            // Page ids of this tile, one per lane.
-            int page = -1;
-            if (lane < n_load) page = a.page_table[it.page_base + j * pages_per_tile + lane];
             const bool bad = lane < n_load && (page < 0 || page >= a.num_pages);
             const unsigned bad_mask = __ballot_sync(0xffffffffu, bad);
             if (bad_mask && lane == 0) atomicOr(a.err, ATTN_DEVICE_ERR_PAGE_ID);
-            const int n_good = n_load - __popc(bad_mask);
+            const int tx = (n_load - __popc(bad_mask)) * box_bytes * (D / 64);
 
             // K tile.
-            const int ks = j % C::kStagesK;
-            if (j >= C::kStagesK &&
-                !__all_sync(0xffffffffu, ptx::mbar_wait(B.k_empty + 8 * ks, ((j / C::kStagesK) - 1) & 1))) {
+            const int ks = jg % C::kStagesK;
+            if (jg >= C::kStagesK && !wait_all(B.k_empty + 8 * ks, ((jg / C::kStagesK) - 1) & 1)) {
                 fail(ATTN_DEVICE_ERR_TIMEOUT);
+                ok = false;
                 break;
             }
-            if (lane == 0) ptx::mbar_arrive_expect_tx(B.k_full + 8 * ks, n_good * box_bytes * (D / 64));
+            if (lane == 0) ptx::mbar_arrive_expect_tx(B.k_full + 8 * ks, tx);
+            // One page box per lane: the boxes of a tile go out in one warp instruction.
             __syncwarp();
-            for (int p = 0; p < n_load; ++p) {
-                const int pg = __shfl_sync(0xffffffffu, page, p);
-                if (lane == 0 && pg >= 0 && pg < a.num_pages)
-                    for (int c = 0; c < D / 64; ++c)
-                        ptx::tma_load_3d_hint(sbase + C::kOffK + ks * C::kTile + c * C::kAtom + p * box_bytes,
-                                              &kv_map, B.k_full + 8 * ks, c * 64, 0,
-                                              (pg * 2) * a.Hkv + it.kv_head, policy);
-            }
+            if (lane < n_load && page >= 0 && page < a.num_pages)
+                for (int c = 0; c < D / 64; ++c)
+                    ptx::tma_load_3d_hint(sbase + C::kOffK + ks * C::kTile + c * C::kAtom + lane * box_bytes,
+                                          &kv_map, B.k_full + 8 * ks, c * 64, 0,
+                                          (page * 2) * a.Hkv + it.kv_head, policy);
+            issued_k = jg + 1;
+
             // V tile.
-            const int vs = j % C::kStagesV;
-            if (j >= C::kStagesV &&
-                !__all_sync(0xffffffffu, ptx::mbar_wait(B.v_empty + 8 * vs, ((j / C::kStagesV) - 1) & 1))) {
+            const int vs = jg % C::kStagesV;
+            if (jg >= C::kStagesV && !wait_all(B.v_empty + 8 * vs, ((jg / C::kStagesV) - 1) & 1)) {
                 fail(ATTN_DEVICE_ERR_TIMEOUT);
+                ok = false;
                 break;
             }
-            const uint32_t vdst = sbase + C::kOffV + vs * C::kTile;
             const bool ragged = valid < kPrefillKeys;
             const uint32_t vbar = ragged ? B.v_aux : B.v_full + 8 * vs;
-            if (lane == 0) ptx::mbar_arrive_expect_tx(vbar, n_good * box_bytes * (D / 64));
+            if (lane == 0) ptx::mbar_arrive_expect_tx(vbar, tx);
             __syncwarp();
-            for (int p = 0; p < n_load; ++p) {
-                const int pg = __shfl_sync(0xffffffffu, page, p);
-                if (lane == 0 && pg >= 0 && pg < a.num_pages)
-                    for (int c = 0; c < D / 64; ++c)
-                        ptx::tma_load_3d_hint(vdst + c * C::kAtom + p * box_bytes, &kv_map, vbar, c * 64, 0,
-                                              (pg * 2 + 1) * a.Hkv + it.kv_head, policy);
-            }
+            if (lane < n_load && page >= 0 && page < a.num_pages)
+                for (int c = 0; c < D / 64; ++c)
+                    ptx::tma_load_3d_hint(sbase + C::kOffV + vs * C::kTile + c * C::kAtom + lane * box_bytes,
+                                          &kv_map, vbar, c * 64, 0, (page * 2 + 1) * a.Hkv + it.kv_head,
+                                          policy);
             if (ragged) {
-                // Only the last tile can be ragged: wait for its rows to land,
-                // zero V rows [valid, 128) (they may hold anything), then
-                // publish the stage to the MMA warp.
-                if (!__all_sync(0xffffffffu, ptx::mbar_wait(B.v_aux, 0))) {
+                // Only an item's last tile can be ragged: wait for its rows,
+                // zero V rows [valid, 128) (they may hold anything), publish.
+                if (!wait_all(B.v_aux, n_aux & 1)) {
                     fail(ATTN_DEVICE_ERR_TIMEOUT);
+                    ok = false;
                     break;
                 }
+                ++n_aux;
                 uint8_t* vrow = smem + C::kOffV + vs * C::kTile;
-                const int n16 = (kPrefillKeys - valid) * 8;     // 16-byte chunks per atom
+                const int n16 = (kPrefillKeys - valid) * 8;   // 16-byte chunks per atom
                 for (int c = 0; c < D / 64; ++c)
                     for (int idx = lane; idx < n16; idx += 32)
-                        *reinterpret_cast<uint4*>(vrow + c * C::kAtom + (valid + idx / 8) * 128 + (idx % 8) * 16) =
-                            make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4*>(vrow + c * C::kAtom + (valid + idx / 8) * 128 +
+                                                  (idx % 8) * 16) = make_uint4(0, 0, 0, 0);
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(B.v_full + 8 * vs);
             }
-            issued = j + 1;
+            issued_v = jg + 1;
+
+            ++jg;
+            if (j_n == 0) ++n_item;
+            item = item_n;
+            j = j_n;
+            it = it_n;
+            page = page_n;
         }
-        if (__any_sync(0xffffffffu, *abort_flag != 0)) {
+        if (!ok) {
             // Let the copies still in flight land before the CTA exits.
-            for (int j = max(0, issued - C::kStagesK); j < issued; ++j)
+            for (int j = max(0, issued_k - C::kStagesK); j < issued_k; ++j)
                 ptx::mbar_wait(B.k_full + 8 * (j % C::kStagesK), (j / C::kStagesK) & 1);
-            for (int j = max(0, issued - C::kStagesV); j < issued; ++j)
+            for (int j = max(0, issued_v - C::kStagesV); j < issued_v; ++j)
                 ptx::mbar_wait(B.v_full + 8 * (j % C::kStagesV), (j / C::kStagesV) & 1);
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == 1 || warp == 2) {
+        // ================================================================ MMA issuers
+        // One issuing thread per head slot, so neither head's MMAs wait behind
+        // the other head's softmax.  Both release the shared K, V and Q stages.
         if (lane == 0) {
+            const int i = warp - 1;
             constexpr uint32_t idesc_qk = ptx::idesc_bf16(128, 128, false, false);
             constexpr uint32_t idesc_pv = ptx::idesc_bf16(128, D, false, true);
-            bool ok = ptx::mbar_wait(B.q_full, 0);
-            for (int j = 0; ok && j < n_tiles; ++j) {
-                const int ks = j % C::kStagesK, vs = j % C::kStagesV;
-                if (!ptx::mbar_wait(B.k_full + 8 * ks, (j / C::kStagesK) & 1)) { ok = false; break; }
-                for (int i = 0; i < nh; ++i) {
-                    if (j > 0 && !ptx::mbar_wait(B.o_done + 8 * i, (j - 1) & 1)) { ok = false; break; }
-                    ptx::tc_fence_after();
-                    const uint32_t qa = sbase + C::kOffQ + i * C::kTile;
-                    const uint32_t kb = sbase + C::kOffK + ks * C::kTile;
+            const uint32_t t_s = tmem + C::kColS + i * 128;
+            const uint32_t t_o = tmem + C::kColO + i * D;
+            const uint32_t t_p = tmem + C::kColP + i * C::kStrideP;
+            int jg = 0, n_item = 0, hj = 0;
+            bool ok = true;
+
+            auto qk = [&](int qb, int ks) {
+                const uint32_t qa = sbase + C::kOffQ + (qb * 2 + i) * C::kTile;
+                const uint32_t kb = sbase + C::kOffK + ks * C::kTile;
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk / 4) * C::kAtom + (kk % 4) * 32;
-                        ptx::tc_mma_ss(tmem + i * 128, ptx::smem_desc_sw128(qa + off, 16, 1024),
-                                       ptx::smem_desc_sw128(kb + off, 16, 1024), idesc_qk, kk > 0);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk / 4) * C::kAtom + (kk % 4) * 32;
+                    ptx::tc_mma_ss(t_s, ptx::smem_desc_sw128(qa + off, 16, 1024),
+                                   ptx::smem_desc_sw128(kb + off, 16, 1024), idesc_qk, kk > 0);
+                }
+                ptx::tc_commit(B.s_full + 8 * i);
+            };
+            auto pv = [&](int vs, bool first) {
+                const uint32_t vb = sbase + C::kOffV + vs * C::kTile;
+#pragma unroll
+                for (int kk = 0; kk < kPrefillKeys / 16; ++kk)
+                    ptx::tc_mma_ts(t_o, t_p + kk * 8, ptx::smem_desc_sw128(vb + kk * 2048, C::kAtom, 1024),
+                                   idesc_pv, (!first || kk > 0) ? 1u : 0u);
+                ptx::tc_commit(B.o_done + 8 * i);
+            };
+            auto kfull = [&](int t) { return ptx::mbar_wait(B.k_full + 8 * (t % C::kStagesK), (t / C::kStagesK) & 1); };
+            auto vfull = [&](int t) { return ptx::mbar_wait(B.v_full + 8 * (t % C::kStagesV), (t / C::kStagesV) & 1); };
+
+            for (int item = blockIdx.x; ok && item < a.n_items; item += gridDim.x, ++n_item) {
+                if (*abort_flag) { ok = false; break; }
+                const PrefillItem it = a.items[item];
+                const int n = it.n_kv_tiles;
+                const int qb = n_item % C::kQBufs;
+                if (!ptx::mbar_wait(B.q_full + 8 * qb, (n_item / C::kQBufs) & 1)) { ok = false; break; }
+                if (i >= it.n_heads) {
+                    // This head slot has no work in the item: only keep the
+                    // shared stages' arrival counts (after each stage is loaded).
+                    for (int j = 0; j < n && ok; ++j) {
+                        const int t = jg + j;
+                        if (!kfull(t)) { ok = false; break; }
+                        ptx::mbar_arrive(B.k_empty + 8 * (t % C::kStagesK));
+                        if (!vfull(t)) { ok = false; break; }
+                        ptx::mbar_arrive(B.v_empty + 8 * (t % C::kStagesV));
                     }
-                    ptx::tc_commit(B.s_full + 8 * i);
+                    ptx::mbar_arrive(B.q_empty + 8 * qb);
+                    jg += n;
+                    continue;
                 }
-                if (!ok) break;
-                ptx::tc_commit(B.k_empty + 8 * ks);
-                if (!ptx::mbar_wait(B.v_full + 8 * vs, (j / C::kStagesV) & 1)) { ok = false; break; }
-                for (int i = 0; i < nh; ++i) {
-                    if (!ptx::mbar_wait(B.p_full + 8 * i, j & 1)) { ok = false; break; }
+                if (C::kSeparateP) {
+                    // QK^T of tile j+1 is issued before PV of tile j.
+                    if (!kfull(jg)) { ok = false; break; }
+                    if (hj > 0 && !ptx::mbar_wait(B.s_free + 8 * i, (hj - 1) & 1)) { ok = false; break; }
                     ptx::tc_fence_after();
-                    const uint32_t vb = sbase + C::kOffV + vs * C::kTile;
-#pragma unroll
-                    for (int kk = 0; kk < kPrefillKeys / 16; ++kk)
-                        ptx::tc_mma_ts(tmem + 256 + i * D, tmem + i * 128 + kk * 8,
-                                       ptx::smem_desc_sw128(vb + kk * 2048, C::kAtom, 1024), idesc_pv,
-                                       (j > 0 || kk > 0) ? 1u : 0u);
-                    ptx::tc_commit(B.o_done + 8 * i);
+                    qk(qb, jg % C::kStagesK);
+                    ptx::tc_commit(B.k_empty + 8 * (jg % C::kStagesK));
+                    if (n == 1) ptx::tc_commit(B.q_empty + 8 * qb);
+                    for (int j = 0; j < n; ++j) {
+                        const int t = jg + j;
+                        if (j + 1 < n) {
+                            if (!kfull(t + 1) || !ptx::mbar_wait(B.s_free + 8 * i, (hj + j) & 1)) { ok = false; break; }
+                            ptx::tc_fence_after();
+                            qk(qb, (t + 1) % C::kStagesK);
+                            ptx::tc_commit(B.k_empty + 8 * ((t + 1) % C::kStagesK));
+                            if (j + 2 == n) ptx::tc_commit(B.q_empty + 8 * qb);
+                        }
+                        if (!vfull(t) || !ptx::mbar_wait(B.p_full + 8 * i, (hj + j) & 1)) { ok = false; break; }
+                        ptx::tc_fence_after();
+                        pv(t % C::kStagesV, j == 0);
+                        ptx::tc_commit(B.v_empty + 8 * (t % C::kStagesV));
+                    }
+                } else {
+                    // P aliases S: QK^T of tile j waits for PV of tile j-1.
+                    for (int j = 0; j < n; ++j) {
+                        const int t = jg + j;
+                        if (!kfull(t)) { ok = false; break; }
+                        if (hj + j > 0 && !ptx::mbar_wait(B.o_done + 8 * i, (hj + j - 1) & 1)) { ok = false; break; }
+                        ptx::tc_fence_after();
+                        qk(qb, t % C::kStagesK);
+                        ptx::tc_commit(B.k_empty + 8 * (t % C::kStagesK));
+                        if (j + 1 == n) ptx::tc_commit(B.q_empty + 8 * qb);
+                        if (!vfull(t) || !ptx::mbar_wait(B.p_full + 8 * i, (hj + j) & 1)) { ok = false; break; }
+                        ptx::tc_fence_after();
+                        pv(t % C::kStagesV, j == 0);
+                        ptx::tc_commit(B.v_empty + 8 * (t % C::kStagesV));
+                    }
                 }
-                if (!ok) break;
-                ptx::tc_commit(B.v_empty + 8 * vs);
+                jg += n;
+                hj += n;
             }
             if (!ok) fail(ATTN_DEVICE_ERR_TIMEOUT);
-            // Arrives once every MMA issued above has finished (tear-down waits on it).
+            // Arrives once every MMA this thread issued has finished.
             ptx::tc_commit(B.drain);
         }
     } else if (warp >= 4) {
-        // ------------------------------------------------------------ softmax
+        // ================================================================ softmax
         ptx::setmaxnreg_inc<C::kRegsSoftmax>();
         const int i = (warp - 4) >> 2;                     // head slot 0 or 1
         const int quad = warp & 3;                         // TMEM lane quadrant of this warp
         const int r = quad * 32 + lane;                    // row within the tile
-        if (i < nh) {
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        const uint32_t t_s = tmem + lane_off + C::kColS + i * 128;
+        const uint32_t t_o = tmem + lane_off + C::kColO + i * D;
+        const uint32_t t_p = tmem + lane_off + C::kColP + i * C::kStrideP;
+        const float sl2 = a.scale_log2;
+        int hj = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; ok && item < a.n_items; item += gridDim.x) {
+            const PrefillItem it = a.items[item];
+            if (i >= it.n_heads) continue;
             const int head = it.head0 + i;
-            const uint32_t t_s = tmem + ((uint32_t)(quad * 32) << 16) + i * 128;
-            const uint32_t t_o = tmem + ((uint32_t)(quad * 32) << 16) + 256 + i * D;
-            const float sl2 = a.scale_log2;
+            const int n = it.n_kv_tiles;
             // l: row sum of the bf16-rounded P that the PV MMA consumes (it
             // normalises O); le: the same sum of the unrounded P (it gives lse).
             float m_use = -INFINITY, l = 0.f, le = 0.f;
@@ -296,9 +423,9 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
             const int last_key = it.kv_len - 1;
             const int row_limit = a.causal ? min(it.pos0 + r, last_key) : last_key;
             const int first_masked = ((a.causal ? min(it.pos0, last_key) : last_key) + 1) / kPrefillKeys;
-            bool ok = true;
-            for (int j = 0; j < n_tiles; ++j) {
-                if (!__all_sync(0xffffffffu, ptx::mbar_wait(B.s_full + 8 * i, j & 1))) { ok = false; break; }
+            for (int j = 0; j < n; ++j) {
+                const int t = hj + j;
+                if (!wait_all(B.s_full + 8 * i, t & 1)) { ok = false; break; }
                 ptx::tc_fence_after();
                 float s[128];
 #pragma unroll
@@ -309,17 +436,29 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                     for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(v[e]);
                 }
                 ptx::tc_wait_ld();
+                if (C::kSeparateP) {
+                    // S is in registers: the MMA warp may overwrite it with the next tile.
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(B.s_free + 8 * i);
+                }
                 if (j >= first_masked) {
                     const int ncol = row_limit - j * kPrefillKeys + 1;
 #pragma unroll
                     for (int c = 0; c < 128; ++c)
                         if (c >= ncol) s[c] = -INFINITY;
                 }
-                float mx = s[0];
+                // Row max: four independent chains of 3-input max.
+                float mq[4];
 #pragma unroll
-                for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
-                const float m_tile = mx * sl2;
-                const float m_new = fmaxf(m_use, m_tile);
+                for (int k = 0; k < 4; ++k) {
+                    mq[k] = s[k * 32];
+#pragma unroll
+                    for (int c = 1; c + 1 < 32; c += 2) mq[k] = ptx::max3(mq[k], s[k * 32 + c], s[k * 32 + c + 1]);
+                    mq[k] = fmaxf(mq[k], s[k * 32 + 31]);
+                }
+                const float mx = ptx::max3(ptx::max3(mq[0], mq[1], mq[2]), mq[3], mq[3]);
+                const float m_new = fmaxf(m_use, mx * sl2);
                 float alpha = 1.f;
                 bool rescale = false;
                 if (m_new > m_use + kRescaleThreshold || (m_use == -INFINITY && m_new != -INFINITY)) {
@@ -329,8 +468,15 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                     m_use = m_new;
                     rescale = j > 0;
                 }
+                // At D = 64 the previous PV must be done before O is touched or
+                // P is overwritten (at D = 128 it is: S of tile j waited for it).
+                bool prev_done = !C::kSeparateP || t == 0;
                 if (__any_sync(0xffffffffu, rescale)) {
-                    // O (complete up to tile j-1) is rescaled in place.
+                    if (!prev_done) {
+                        if (!wait_all(B.o_done + 8 * i, (t - 1) & 1)) { ok = false; break; }
+                        prev_done = true;
+                        ptx::tc_fence_after();
+                    }
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t v[32];
@@ -342,64 +488,69 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                     }
                 }
                 const float neg_m = m_use == -INFINITY ? 0.f : -m_use;
-                float ls0 = 0.f, ls1 = 0.f, le0 = 0.f, le1 = 0.f;
+                const float2 sl2x2 = make_float2(sl2, sl2), negm2 = make_float2(neg_m, neg_m);
+                float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                float2 lx2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                uint32_t pk[2][32];
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
-                    uint32_t pk[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
-                        const float p0 = ptx::ex2(fmaf(s[c * 64 + 2 * e], sl2, neg_m));
-                        const float p1 = ptx::ex2(fmaf(s[c * 64 + 2 * e + 1], sl2, neg_m));
-                        pk[e] = ptx::pack_bf16x2(p0, p1);
-                        const float2 pr = ptx::unpack_bf16x2(pk[e]);
-                        ls0 += pr.x;
-                        ls1 += pr.y;
-                        le0 += p0;
-                        le1 += p1;
+                        const float2 x = ptx::fma2(make_float2(s[c * 64 + 2 * e], s[c * 64 + 2 * e + 1]), sl2x2, negm2);
+                        const float2 p = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
+                        pk[c][e] = ptx::pack_bf16x2(p.x, p.y);
+                        ls2[e & 1] = ptx::add2(ls2[e & 1], ptx::unpack_bf16x2(pk[c][e]));
+                        lx2[e & 1] = ptx::add2(lx2[e & 1], p);
                     }
-                    ptx::tmem_st32(t_s + c * 32, pk);
                 }
-                l += ls0 + ls1;
-                le += le0 + le1;
+                const float2 lsum = ptx::add2(ls2[0], ls2[1]), lxsum = ptx::add2(lx2[0], lx2[1]);
+                l += lsum.x + lsum.y;
+                le += lxsum.x + lxsum.y;
+                if (!prev_done) {
+                    if (!wait_all(B.o_done + 8 * i, (t - 1) & 1)) { ok = false; break; }
+                    ptx::tc_fence_after();
+                }
+                ptx::tmem_st32(t_p, pk[0]);
+                ptx::tmem_st32(t_p + 32, pk[1]);
                 ptx::tc_wait_st();
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(B.p_full + 8 * i);
             }
-            if (ok && !__all_sync(0xffffffffu, ptx::mbar_wait(B.o_done + 8 * i, (n_tiles - 1) & 1))) ok = false;
-            if (!ok) {
-                fail(ATTN_DEVICE_ERR_TIMEOUT);
-            } else {
-                ptx::tc_fence_after();
-                const float inv = l > 0.f ? 1.f / l : 0.f;
-                const bool store = r < it.n_rows;
-                __nv_bfloat16* orow = a.out + ((size_t)(it.q_row0 + r) * a.Hq + head) * D;
+            if (!ok) break;
+            // Epilogue: O of this item is complete once the last PV is done.
+            if (!wait_all(B.o_done + 8 * i, (hj + n - 1) & 1)) { ok = false; break; }
+            ptx::tc_fence_after();
+            hj += n;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const bool store = r < it.n_rows;
+            __nv_bfloat16* orow = a.out + ((size_t)(it.q_row0 + r) * a.Hq + head) * D;
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t v[32];
-                    ptx::tmem_ld32(t_o + c * 32, v);
-                    ptx::tc_wait_ld();
-                    if (store) {
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t v[32];
+                ptx::tmem_ld32(t_o + c * 32, v);
+                ptx::tc_wait_ld();
+                if (store) {
 #pragma unroll
-                        for (int e = 0; e < 32; e += 8) {
-                            uint4 w;
-                            w.x = ptx::pack_bf16x2(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv);
-                            w.y = ptx::pack_bf16x2(__uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv);
-                            w.z = ptx::pack_bf16x2(__uint_as_float(v[e + 4]) * inv, __uint_as_float(v[e + 5]) * inv);
-                            w.w = ptx::pack_bf16x2(__uint_as_float(v[e + 6]) * inv, __uint_as_float(v[e + 7]) * inv);
-                            *reinterpret_cast<uint4*>(orow + c * 32 + e) = w;
-                        }
+                    for (int e = 0; e < 32; e += 8) {
+                        uint4 w;
+                        w.x = ptx::pack_bf16x2(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv);
+                        w.y = ptx::pack_bf16x2(__uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv);
+                        w.z = ptx::pack_bf16x2(__uint_as_float(v[e + 4]) * inv, __uint_as_float(v[e + 5]) * inv);
+                        w.w = ptx::pack_bf16x2(__uint_as_float(v[e + 6]) * inv, __uint_as_float(v[e + 7]) * inv);
+                        *reinterpret_cast<uint4*>(orow + c * 32 + e) = w;
                     }
                 }
-                if (store && a.lse)
-                    a.lse[(size_t)(it.q_row0 + r) * a.Hq + head] =
-                        le > 0.f ? (m_use + log2f(le)) * kLn2 : -INFINITY;
             }
+            if (store && a.lse)
+                a.lse[(size_t)(it.q_row0 + r) * a.Hq + head] =
+                    le > 0.f ? (m_use + log2f(le)) * kLn2 : -INFINITY;
         }
+        if (!ok) fail(ATTN_DEVICE_ERR_TIMEOUT);
     }
 
-    // Tear-down: every TMEM access and MMA is complete (the softmax warps
-    // waited for the last PV of their head), so the columns can be released.
+    // Tear-down: each MMA thread's last commit arrives on `drain` once every
+    // MMA it issued is complete; then the TMEM columns are released.
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -411,7 +562,7 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
 }
 
 template <int D>
-cudaError_t launch(const CUtensorMap& qm, const CUtensorMap& km, const PrefillArgs& args, int n,
+cudaError_t launch(const CUtensorMap& qm, const CUtensorMap& km, const PrefillArgs& args, int grid,
                    cudaStream_t stream) {
     using C = PrefillCfg<D>;
     auto kernel = prefill_sink_attn_kernel<D>;
@@ -426,7 +577,7 @@ cudaError_t launch(const CUtensorMap& qm, const CUtensorMap& km, const PrefillAr
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    kernel<<<n, C::kThreads, C::kSmem, stream>>>(qm, km, args);
+    kernel<<<grid, C::kThreads, C::kSmem, stream>>>(qm, km, args);
     return cudaGetLastError();
 }
 
@@ -437,6 +588,7 @@ attn_status launch_prefill(attn_plan_s* plan, const void* q_map, const void* kv_
     if (plan->items.empty()) return ATTN_OK;
     PrefillArgs a;
     a.items = reinterpret_cast<const PrefillItem*>(plan->ws + plan->layout.items);
+    a.n_items = (int32_t)plan->items.size();
     a.page_table = plan->page_table;
     a.out = static_cast<__nv_bfloat16*>(out);
     a.lse = lse;
@@ -450,8 +602,9 @@ attn_status launch_prefill(attn_plan_s* plan, const void* q_map, const void* kv_
     a.scale_log2 = plan->sm_scale * kLog2e;
     const CUtensorMap& qm = *static_cast<const CUtensorMap*>(q_map);
     const CUtensorMap& km = *static_cast<const CUtensorMap*>(kv_map);
-    const int n = (int)plan->items.size();
-    const cudaError_t e = plan->D == 64 ? launch<64>(qm, km, a, n, stream) : launch<128>(qm, km, a, n, stream);
+    // Persistent grid: one CTA per SM (the kernel needs all of an SM's TMEM).
+    const int grid = a.n_items < plan->num_sms ? a.n_items : plan->num_sms;
+    const cudaError_t e = plan->D == 64 ? launch<64>(qm, km, a, grid, stream) : launch<128>(qm, km, a, grid, stream);
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -135,3 +135,18 @@ def test_prefill_bitwise_deterministic():
     torch.cuda.synchronize()
     for o, l in res[1:]:
         assert torch.equal(o, res[0][0]) and torch.equal(l, res[0][1])
+
+
+@pytest.mark.parametrize("num_sms", [1, 3, 152])
+def test_prefill_persistent_item_streams(num_sms):
+    """Few CTAs walk long item lists (mixed head counts, ragged and full
+    tiles), so barrier phases carry across many items per CTA."""
+    batch = syn.make_batch("persist", [300, 129, 2, 700], [300, 400, 2, 900], 12, 4, 64, 16, seed=11)
+    q, kv, pt, sk = to_device(batch)
+    plan = make_plan(batch, pt, num_sms=num_sms)
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full((batch.total_rows, batch.num_qo_heads), float("nan"), device="cuda")
+    plan.prefill(q, kv, sk, out, lse)
+    torch.cuda.synchronize()
+    assert plan.device_error() == 0
+    _check_rows(batch, out, lse, what=f"sms={num_sms}")
