@@ -84,8 +84,10 @@ extern "C" attn_status attn_plan_bind_workspace(attn_plan_t plan, void* workspac
                         cudaMemcpyHostToDevice, s) != cudaSuccess)
         return ATTN_ERR_CUDA;
     if (!plan->items.empty() &&
-        cudaMemcpyAsync(ws + L.items, plan->items.data(), plan->items.size() * sizeof(attn::PrefillItem),
-                        cudaMemcpyHostToDevice, s) != cudaSuccess)
+        (cudaMemcpyAsync(ws + L.items, plan->items.data(), plan->items.size() * sizeof(attn::PrefillItem),
+                         cudaMemcpyHostToDevice, s) != cudaSuccess ||
+         cudaMemcpyAsync(ws + L.item_off, plan->item_off.data(), plan->item_off.size() * sizeof(int32_t),
+                         cudaMemcpyHostToDevice, s) != cudaSuccess))
         return ATTN_ERR_CUDA;
     // counters and the error word are adjacent: clear both.
     if (cudaMemsetAsync(ws + L.counters, 0, L.part_lse - L.counters, s) != cudaSuccess) return ATTN_ERR_CUDA;

@@ -47,7 +47,7 @@ struct PrefillItem {
     int32_t kv_head;
     int32_t head0;
     int32_t n_heads;     // 1 or 2
-    int32_t n_kv_tiles;  // 128-key tiles visited
+    int32_t n_kv_tiles;  // 128-key KV tiles visited
     int32_t key_end;     // one past the last key any row of the tile may see
     int32_t reserved0;
     int32_t reserved1;
@@ -55,7 +55,7 @@ struct PrefillItem {
 static_assert(sizeof(PrefillItem) == 48, "prefill item is 12 int32");
 
 struct WorkspaceLayout {
-    size_t units = 0, items = 0, counters = 0, err = 0, part_lse = 0, part_o = 0, total = 0;
+    size_t units = 0, items = 0, item_off = 0, counters = 0, err = 0, part_lse = 0, part_o = 0, total = 0;
 };
 
 // CTAs of the decode kernel resident per SM for a head dim (matches its
@@ -73,6 +73,8 @@ struct attn_plan_s {
 
     std::vector<attn::DecodeUnit> units;
     std::vector<attn::PrefillItem> items;
+    std::vector<int32_t> item_off;        // CTA c runs items [item_off[c], item_off[c+1])
+    int32_t prefill_ctas = 0;
     int32_t n_groups = 0;
     int32_t n_partials = 0;
     attn_plan_info info{};

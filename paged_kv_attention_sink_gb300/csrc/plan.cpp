@@ -36,7 +36,7 @@ extern "C" attn_status attn_plan(const int32_t* qo_indptr, const int32_t* kv_ind
     if (num_qo_heads <= 0 || num_kv_heads <= 0 || num_qo_heads % num_kv_heads != 0)
         return ATTN_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
-    if (!std::isfinite(sm_scale)) return ATTN_ERR_INVALID_ARG;
+    if (!std::isfinite(sm_scale) || !(sm_scale > 0.f)) return ATTN_ERR_INVALID_ARG;
     if (head_dim <= 0 || page_size <= 0 || num_sms < 0) return ATTN_ERR_INVALID_ARG;
     if (!supported_head_dim(head_dim) || !supported_page_size(page_size)) return ATTN_ERR_UNSUPPORTED;
 
@@ -143,7 +143,8 @@ extern "C" attn_status attn_plan(const int32_t* qo_indptr, const int32_t* kv_ind
                          return (a.tok_end - a.tok_begin) > (b.tok_end - b.tok_begin);
                      });
 
-    // ---- prefill: one item per (128-row tile, pair of query heads of a group).
+    // ---- prefill: one item per (128-row tile, pair of query heads of a group),
+    // visiting 128-key KV tiles up to the causal diagonal.
     for (int32_t b = 0; b < batch; ++b) {
         if (qo_len[b] <= 1) continue;
         const int64_t prefix = kv_len[b] - qo_len[b];
@@ -171,16 +172,42 @@ extern "C" attn_status attn_plan(const int32_t* qo_indptr, const int32_t* kv_ind
             }
         }
     }
+    // Persistent prefill CTAs: greedy longest-processing-time assignment of
+    // the items (longest first, each to the least-loaded CTA); each CTA's items
+    // are stored contiguously, longest first.
     std::stable_sort(plan->items.begin(), plan->items.end(),
                      [](const PrefillItem& a, const PrefillItem& b) {
                          return a.n_kv_tiles * a.n_heads > b.n_kv_tiles * b.n_heads;
                      });
+    if (!plan->items.empty()) {
+        const int ctas = (int)std::min<int64_t>(num_sms, (int64_t)plan->items.size());
+        std::vector<std::vector<PrefillItem>> per(ctas);
+        std::vector<std::pair<int64_t, int>> heap;   // (load, cta), min-heap
+        for (int c = 0; c < ctas; ++c) heap.push_back({0, c});
+        auto cmp = [](const std::pair<int64_t, int>& x, const std::pair<int64_t, int>& y) { return x > y; };
+        std::make_heap(heap.begin(), heap.end(), cmp);
+        for (const PrefillItem& it : plan->items) {
+            std::pop_heap(heap.begin(), heap.end(), cmp);
+            auto& least = heap.back();
+            per[least.second].push_back(it);
+            least.first += (int64_t)it.n_kv_tiles * it.n_heads + 1;   // +1: per-item overhead
+            std::push_heap(heap.begin(), heap.end(), cmp);
+        }
+        plan->items.clear();
+        plan->item_off.assign(1, 0);
+        for (int c = 0; c < ctas; ++c) {
+            plan->items.insert(plan->items.end(), per[c].begin(), per[c].end());
+            plan->item_off.push_back((int32_t)plan->items.size());
+        }
+        plan->prefill_ctas = ctas;
+    }
 
     // ---- workspace layout (every region 256-byte aligned).
     WorkspaceLayout& L = plan->layout;
     size_t off = 0;
     L.units = off;    off = align_up(off + plan->units.size() * sizeof(DecodeUnit), 256);
     L.items = off;    off = align_up(off + plan->items.size() * sizeof(PrefillItem), 256);
+    L.item_off = off; off = align_up(off + plan->item_off.size() * sizeof(int32_t), 256);
     L.counters = off; off = align_up(off + (size_t)plan->n_groups * sizeof(int32_t), 256);
     L.err = off;      off = align_up(off + sizeof(int32_t), 256);
     L.part_lse = off; off = align_up(off + (size_t)plan->n_partials * kMaxSliceHeads * sizeof(float), 256);

@@ -8,15 +8,16 @@
 // fp32 accumulators in tensor memory.
 //
 // Work item = 128 query rows of one request x two query heads of one GQA group
-// (both heads share every K/V tile).  The grid is persistent: one CTA per SM
-// walks the planner's longest-first item list with a stride of gridDim.x, so
-// the next item's Q and K/V loads and QK^T overlap the current item's last
+// (both heads share every K/V tile).  The grid is persistent: CTA c walks the
+// items the planner assigned to it (greedy longest-processing-time), so the
+// next item's Q and K/V loads and QK^T overlap the current item's last
 // softmax and epilogue.  Roles (12 warps = 3 warpgroups):
 //
-//  * warp 0: TMA producer.  Q tiles (double-buffered at D = 64), K and V rings
-//    of 128-key tiles, one box per HND page issued by its own lane (the
-//    boxes of a tile leave in one warp instruction), 128-byte swizzled.  V rows past
-//    the end of the sequence are zeroed before the MMA may read them.
+//  * warps 0 and 3: TMA producers, warp 0 for Q (double-buffered at D = 64)
+//    and the K ring, warp 3 for the V ring, each walking the tiles on its own.
+//    Tiles are 128 keys; one box per HND page, issued by its own lane (the
+//    boxes of a tile leave in one warp instruction), 128-byte swizzled.  V rows
+//    past the end of the sequence are zeroed before the MMA may read them.
 //  * warps 1 and 2, one lane each: tcgen05.mma issuers, one per head slot
 //    (neither head's MMAs queue behind the other's softmax).  S_h = Q_h K^T (both operands
 //    K-major in shared memory); O_h += P_h V with P read from tensor memory
@@ -27,7 +28,6 @@
 //    the running max is raised lazily (O is rescaled in TMEM only when the max
 //    grew by more than 2^8); P is rounded to bf16 and O is normalised by the
 //    row sum of that rounded P, while lse uses the unrounded sum.
-//  * warp 3 idle (it keeps warpgroup 0 whole for setmaxnreg).
 //
 // TMEM (512 columns): S0 S1 (128 each), O0 O1 (D each), and at D = 64 P0 P1
 // (64 each); at D = 128 P aliases the first half of S.
@@ -76,7 +76,7 @@ struct PrefillCfg {
 
 struct PrefillArgs {
     const PrefillItem* items;
-    int32_t n_items;
+    const int32_t* item_off;     // CTA c runs items [item_off[c], item_off[c+1])
     const int32_t* page_table;
     __nv_bfloat16* out;
     float* lse;
@@ -124,6 +124,7 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
     B.drain = B.v_aux + 8;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int item_begin = a.item_off[blockIdx.x], item_end = a.item_off[blockIdx.x + 1];
 
     if (tid == 0) {
         // The "empty" barriers and `drain` take one arrival from each of the
@@ -169,40 +170,45 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
 
     if (warp < 4) ptx::setmaxnreg_dec<C::kRegsCtrl>();
 
-    if (warp == 0) {
-        // ================================================================ producer
+    if (warp == 0 || warp == 3) {
+        // ================================================================ producers
+        // Warp 0 loads Q and K, warp 3 loads V: two independent walks over this
+        // CTA's tiles, so a K tile never waits behind a V stage (or vice versa).
+        const bool is_k = warp == 0;
         const int P = a.P;
         const int pages_per_tile = kPrefillKeys / P;
         const int box_bytes = P * 128;               // P rows x 64 bf16
+        const int n_stages = is_k ? C::kStagesK : C::kStagesV;
+        const uint32_t full0 = is_k ? B.k_full : B.v_full;
+        const uint32_t empty0 = is_k ? B.k_empty : B.v_empty;
+        const uint32_t dst0 = sbase + (is_k ? C::kOffK : C::kOffV);
         const uint64_t policy = ptx::policy_evict_last();
-        int jg = 0, n_item = 0, n_aux = 0;
-        int issued_k = 0, issued_v = 0;
+        int jg = 0, n_item = 0, n_aux = 0, issued = 0;
         bool ok = true;
-        // The producer walks this CTA's tiles (item, j) in order.  The page ids
-        // of the next tile are loaded (one per lane) while the current tile is
-        // issued, so the dependent global load never sits between two tiles.
+        // The page ids of the next tile are loaded (one per lane) while the
+        // current tile is issued, so the dependent global load never sits
+        // between two tiles.
         auto n_load_of = [&](const PrefillItem& x, int j) {
             return (min(kPrefillKeys, x.kv_len - j * kPrefillKeys) + P - 1) / P;
         };
         auto load_pages = [&](const PrefillItem& x, int j) {
             return lane < n_load_of(x, j) ? a.page_table[x.page_base + j * pages_per_tile + lane] : -1;
         };
-        int item = blockIdx.x, j = 0;
+        int item = item_begin, j = 0;
         PrefillItem it = a.items[item];
         int page = load_pages(it, 0);
-        while (item < a.n_items) {
+        while (item < item_end) {
             if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
-            // Next tile of the walk and its page ids.
             int item_n = item, j_n = j + 1;
             PrefillItem it_n = it;
             if (j_n == it.n_kv_tiles) {
-                item_n = item + gridDim.x;
+                item_n = item + 1;
                 j_n = 0;
-                if (item_n < a.n_items) it_n = a.items[item_n];
+                if (item_n < item_end) it_n = a.items[item_n];
             }
-            const int page_n = item_n < a.n_items ? load_pages(it_n, j_n) : -1;
+            const int page_n = item_n < item_end ? load_pages(it_n, j_n) : -1;
 
-            if (j == 0) {
+            if (is_k && j == 0) {
                 const int qb = n_item % C::kQBufs;
                 if (n_item >= C::kQBufs && !wait_all(B.q_empty + 8 * qb, ((n_item / C::kQBufs) - 1) & 1)) {
                     fail(ATTN_DEVICE_ERR_TIMEOUT);
@@ -224,39 +230,23 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
             if (bad_mask && lane == 0) atomicOr(a.err, ATTN_DEVICE_ERR_PAGE_ID);
             const int tx = (n_load - __popc(bad_mask)) * box_bytes * (D / 64);
 
-            // K tile.
-            const int ks = jg % C::kStagesK;
-            if (jg >= C::kStagesK && !wait_all(B.k_empty + 8 * ks, ((jg / C::kStagesK) - 1) & 1)) {
+            const int st = jg % n_stages;
+            if (jg >= n_stages && !wait_all(empty0 + 8 * st, ((jg / n_stages) - 1) & 1)) {
                 fail(ATTN_DEVICE_ERR_TIMEOUT);
                 ok = false;
                 break;
             }
-            if (lane == 0) ptx::mbar_arrive_expect_tx(B.k_full + 8 * ks, tx);
-            // One page box per lane: the boxes of a tile go out in one warp instruction.
+            // V rows past the end of the sequence must be zeroed before the MMA
+            // may read them, so a ragged V tile lands on `v_aux` first.
+            const bool ragged = !is_k && valid < kPrefillKeys;
+            const uint32_t bar = ragged ? B.v_aux : full0 + 8 * st;
+            if (lane == 0) ptx::mbar_arrive_expect_tx(bar, tx);
+            // One page box per lane: the boxes of a tile leave in one warp instruction.
             __syncwarp();
             if (lane < n_load && page >= 0 && page < a.num_pages)
                 for (int c = 0; c < D / 64; ++c)
-                    ptx::tma_load_3d_hint(sbase + C::kOffK + ks * C::kTile + c * C::kAtom + lane * box_bytes,
-                                          &kv_map, B.k_full + 8 * ks, c * 64, 0,
-                                          (page * 2) * a.Hkv + it.kv_head, policy);
-            issued_k = jg + 1;
-
-            // V tile.
-            const int vs = jg % C::kStagesV;
-            if (jg >= C::kStagesV && !wait_all(B.v_empty + 8 * vs, ((jg / C::kStagesV) - 1) & 1)) {
-                fail(ATTN_DEVICE_ERR_TIMEOUT);
-                ok = false;
-                break;
-            }
-            const bool ragged = valid < kPrefillKeys;
-            const uint32_t vbar = ragged ? B.v_aux : B.v_full + 8 * vs;
-            if (lane == 0) ptx::mbar_arrive_expect_tx(vbar, tx);
-            __syncwarp();
-            if (lane < n_load && page >= 0 && page < a.num_pages)
-                for (int c = 0; c < D / 64; ++c)
-                    ptx::tma_load_3d_hint(sbase + C::kOffV + vs * C::kTile + c * C::kAtom + lane * box_bytes,
-                                          &kv_map, vbar, c * 64, 0, (page * 2 + 1) * a.Hkv + it.kv_head,
-                                          policy);
+                    ptx::tma_load_3d_hint(dst0 + st * C::kTile + c * C::kAtom + lane * box_bytes, &kv_map, bar,
+                                          c * 64, 0, (page * 2 + (is_k ? 0 : 1)) * a.Hkv + it.kv_head, policy);
             if (ragged) {
                 // Only an item's last tile can be ragged: wait for its rows,
                 // zero V rows [valid, 128) (they may hold anything), publish.
@@ -266,17 +256,17 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                     break;
                 }
                 ++n_aux;
-                uint8_t* vrow = smem + C::kOffV + vs * C::kTile;
+                uint8_t* vrow = smem + C::kOffV + st * C::kTile;
                 const int n16 = (kPrefillKeys - valid) * 8;   // 16-byte chunks per atom
                 for (int c = 0; c < D / 64; ++c)
                     for (int idx = lane; idx < n16; idx += 32)
-                        *reinterpret_cast<uint4*>(vrow + c * C::kAtom + (valid + idx / 8) * 128 +
-                                                  (idx % 8) * 16) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4*>(vrow + c * C::kAtom + (valid + idx / 8) * 128 + (idx % 8) * 16) =
+                            make_uint4(0, 0, 0, 0);
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(B.v_full + 8 * vs);
+                if (lane == 0) ptx::mbar_arrive(B.v_full + 8 * st);
             }
-            issued_v = jg + 1;
+            issued = jg + 1;
 
             ++jg;
             if (j_n == 0) ++n_item;
@@ -287,10 +277,8 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
         }
         if (!ok) {
             // Let the copies still in flight land before the CTA exits.
-            for (int j = max(0, issued_k - C::kStagesK); j < issued_k; ++j)
-                ptx::mbar_wait(B.k_full + 8 * (j % C::kStagesK), (j / C::kStagesK) & 1);
-            for (int j = max(0, issued_v - C::kStagesV); j < issued_v; ++j)
-                ptx::mbar_wait(B.v_full + 8 * (j % C::kStagesV), (j / C::kStagesV) & 1);
+            for (int t = max(0, issued - n_stages); t < issued; ++t)
+                ptx::mbar_wait(full0 + 8 * (t % n_stages), (t / n_stages) & 1);
         }
     } else if (warp == 1 || warp == 2) {
         // ================================================================ MMA issuers
@@ -328,7 +316,7 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
             auto kfull = [&](int t) { return ptx::mbar_wait(B.k_full + 8 * (t % C::kStagesK), (t / C::kStagesK) & 1); };
             auto vfull = [&](int t) { return ptx::mbar_wait(B.v_full + 8 * (t % C::kStagesV), (t / C::kStagesV) & 1); };
 
-            for (int item = blockIdx.x; ok && item < a.n_items; item += gridDim.x, ++n_item) {
+            for (int item = item_begin; ok && item < item_end; ++item, ++n_item) {
                 if (*abort_flag) { ok = false; break; }
                 const PrefillItem it = a.items[item];
                 const int n = it.n_kv_tiles;
@@ -406,7 +394,7 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
         const float sl2 = a.scale_log2;
         int hj = 0;
         bool ok = true;
-        for (int item = blockIdx.x; ok && item < a.n_items; item += gridDim.x) {
+        for (int item = item_begin; ok && item < item_end; ++item) {
             const PrefillItem it = a.items[item];
             if (i >= it.n_heads) continue;
             const int head = it.head0 + i;
@@ -448,16 +436,15 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                     for (int c = 0; c < 128; ++c)
                         if (c >= ncol) s[c] = -INFINITY;
                 }
-                // Row max: four independent chains of 3-input max.
-                float mq[4];
+                // Row max: 16 independent chains of 3-input max, then a tree.
+                float mq[16];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    mq[k] = s[k * 32];
+                for (int k = 0; k < 16; ++k)
+                    mq[k] = ptx::max3(ptx::max3(s[k], s[16 + k], s[32 + k]), ptx::max3(s[48 + k], s[64 + k], s[80 + k]),
+                                      ptx::max3(s[96 + k], s[112 + k], s[112 + k]));
 #pragma unroll
-                    for (int c = 1; c + 1 < 32; c += 2) mq[k] = ptx::max3(mq[k], s[k * 32 + c], s[k * 32 + c + 1]);
-                    mq[k] = fmaxf(mq[k], s[k * 32 + 31]);
-                }
-                const float mx = ptx::max3(ptx::max3(mq[0], mq[1], mq[2]), mq[3], mq[3]);
+                for (int k = 0; k < 5; ++k) mq[k] = ptx::max3(mq[k], mq[5 + k], mq[10 + k]);
+                const float mx = ptx::max3(ptx::max3(mq[0], mq[1], mq[2]), ptx::max3(mq[3], mq[4], mq[15]), mq[15]);
                 const float m_new = fmaxf(m_use, mx * sl2);
                 float alpha = 1.f;
                 bool rescale = false;
@@ -588,7 +575,7 @@ attn_status launch_prefill(attn_plan_s* plan, const void* q_map, const void* kv_
     if (plan->items.empty()) return ATTN_OK;
     PrefillArgs a;
     a.items = reinterpret_cast<const PrefillItem*>(plan->ws + plan->layout.items);
-    a.n_items = (int32_t)plan->items.size();
+    a.item_off = reinterpret_cast<const int32_t*>(plan->ws + plan->layout.item_off);
     a.page_table = plan->page_table;
     a.out = static_cast<__nv_bfloat16*>(out);
     a.lse = lse;
@@ -602,8 +589,9 @@ attn_status launch_prefill(attn_plan_s* plan, const void* q_map, const void* kv_
     a.scale_log2 = plan->sm_scale * kLog2e;
     const CUtensorMap& qm = *static_cast<const CUtensorMap*>(q_map);
     const CUtensorMap& km = *static_cast<const CUtensorMap*>(kv_map);
-    // Persistent grid: one CTA per SM (the kernel needs all of an SM's TMEM).
-    const int grid = a.n_items < plan->num_sms ? a.n_items : plan->num_sms;
+    // Persistent grid: one CTA per planned item list (at most one per SM; the
+    // kernel holds all of an SM's TMEM).
+    const int grid = plan->prefill_ctas;
     const cudaError_t e = plan->D == 64 ? launch<64>(qm, km, a, grid, stream) : launch<128>(qm, km, a, grid, stream);
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
