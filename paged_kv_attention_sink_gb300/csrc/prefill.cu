@@ -25,9 +25,10 @@
 //    columns, so S_h of tile j+1 is computed while the softmax of tile j runs.
 //  * warps 4-7 / 8-11: softmax of head 0 / head 1, one thread per query row
 //    (= TMEM lane).  Causal / length mask on diagonal and ragged tiles only;
-//    the running max is raised lazily (O is rescaled in TMEM only when the max
-//    grew by more than 2^8); P is rounded to bf16 and O is normalised by the
-//    row sum of that rounded P, while lse uses the unrounded sum.
+//    the row max is taken on an item's first tile only; later tiles keep it
+//    unless their P row sum passes 2^64 (then the max is raised, O rescaled in
+//    TMEM and the tile recomputed); P is rounded to bf16 and O is normalised
+//    by the row sum of that rounded P, while lse uses the unrounded sum.
 //
 // TMEM (512 columns): S0 S1 (128 each), O0 O1 (D each), and at D = 64 P0 P1
 // (64 each); at D = 128 P aliases the first half of S.
@@ -43,7 +44,7 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleThreshold = 8.0f;   // log2 units: P stays <= 2^8 between rescales
+constexpr float kSumLimit = 18446744073709551616.0f;   // 2^64: tile row sum that forces a new max
 
 template <int D>
 struct PrefillCfg {
@@ -437,28 +438,62 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                         if (c >= ncol) s[c] = -INFINITY;
                 }
                 // Row max: 16 independent chains of 3-input max, then a tree.
-                float mq[16];
+                auto row_max = [&]() {
+                    float mq[16];
 #pragma unroll
-                for (int k = 0; k < 16; ++k)
-                    mq[k] = ptx::max3(ptx::max3(s[k], s[16 + k], s[32 + k]), ptx::max3(s[48 + k], s[64 + k], s[80 + k]),
-                                      ptx::max3(s[96 + k], s[112 + k], s[112 + k]));
+                    for (int k = 0; k < 16; ++k)
+                        mq[k] = ptx::max3(ptx::max3(s[k], s[16 + k], s[32 + k]),
+                                          ptx::max3(s[48 + k], s[64 + k], s[80 + k]),
+                                          ptx::max3(s[96 + k], s[112 + k], s[112 + k]));
 #pragma unroll
-                for (int k = 0; k < 5; ++k) mq[k] = ptx::max3(mq[k], mq[5 + k], mq[10 + k]);
-                const float mx = ptx::max3(ptx::max3(mq[0], mq[1], mq[2]), ptx::max3(mq[3], mq[4], mq[15]), mq[15]);
-                const float m_new = fmaxf(m_use, mx * sl2);
-                float alpha = 1.f;
-                bool rescale = false;
-                if (m_new > m_use + kRescaleThreshold || (m_use == -INFINITY && m_new != -INFINITY)) {
-                    alpha = ptx::ex2(m_use - m_new);
+                    for (int k = 0; k < 5; ++k) mq[k] = ptx::max3(mq[k], mq[5 + k], mq[10 + k]);
+                    return ptx::max3(ptx::max3(mq[0], mq[1], mq[2]), ptx::max3(mq[3], mq[4], mq[15]), mq[15]);
+                };
+                // Raise the running max to cover this tile; returns the factor
+                // that rescales the state accumulated so far.
+                auto raise_max = [&]() {
+                    const float m_new = fmaxf(m_use, row_max() * sl2);
+                    const float alpha = m_new > m_use ? ptx::ex2(m_use - m_new) : 1.f;
                     l *= alpha;
                     le *= alpha;
                     m_use = m_new;
-                    rescale = j > 0;
-                }
+                    return alpha;
+                };
+                // The first tile of an item sets the running max.  Later tiles
+                // reuse it and skip the max: P = 2^(s - m) is computed directly,
+                // and only when the tile's row sum exceeds 2^64 (some P could
+                // then be large enough to overflow the sums) is the max raised,
+                // O rescaled and the tile recomputed.  Any max is a valid
+                // softmax shift, so the result does not depend on when it moves.
+                if (j == 0) raise_max();
                 // At D = 64 the previous PV must be done before O is touched or
                 // P is overwritten (at D = 128 it is: S of tile j waited for it).
                 bool prev_done = !C::kSeparateP || t == 0;
-                if (__any_sync(0xffffffffu, rescale)) {
+                uint32_t pk[2][32];
+                float tile_l = 0.f, tile_le = 0.f;
+#pragma unroll 1
+                for (int pass = 0;; ++pass) {
+                    const float neg_m = m_use == -INFINITY ? 0.f : -m_use;
+                    const float2 sl2x2 = make_float2(sl2, sl2), negm2 = make_float2(neg_m, neg_m);
+                    float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                    float2 lx2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const float2 x =
+                                ptx::fma2(make_float2(s[c * 64 + 2 * e], s[c * 64 + 2 * e + 1]), sl2x2, negm2);
+                            const float2 p = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
+                            pk[c][e] = ptx::pack_bf16x2(p.x, p.y);
+                            ls2[e & 1] = ptx::add2(ls2[e & 1], ptx::unpack_bf16x2(pk[c][e]));
+                            lx2[e & 1] = ptx::add2(lx2[e & 1], p);
+                        }
+                    }
+                    const float2 lsum = ptx::add2(ls2[0], ls2[1]), lxsum = ptx::add2(lx2[0], lx2[1]);
+                    tile_l = lsum.x + lsum.y;
+                    tile_le = lxsum.x + lxsum.y;
+                    if (j == 0 || pass > 0 || !__any_sync(0xffffffffu, tile_le > kSumLimit)) break;
+                    const float alpha = raise_max();
                     if (!prev_done) {
                         if (!wait_all(B.o_done + 8 * i, (t - 1) & 1)) { ok = false; break; }
                         prev_done = true;
@@ -474,25 +509,9 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                         ptx::tmem_st32(t_o + c * 32, v);
                     }
                 }
-                const float neg_m = m_use == -INFINITY ? 0.f : -m_use;
-                const float2 sl2x2 = make_float2(sl2, sl2), negm2 = make_float2(neg_m, neg_m);
-                float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-                float2 lx2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-                uint32_t pk[2][32];
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const float2 x = ptx::fma2(make_float2(s[c * 64 + 2 * e], s[c * 64 + 2 * e + 1]), sl2x2, negm2);
-                        const float2 p = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
-                        pk[c][e] = ptx::pack_bf16x2(p.x, p.y);
-                        ls2[e & 1] = ptx::add2(ls2[e & 1], ptx::unpack_bf16x2(pk[c][e]));
-                        lx2[e & 1] = ptx::add2(lx2[e & 1], p);
-                    }
-                }
-                const float2 lsum = ptx::add2(ls2[0], ls2[1]), lxsum = ptx::add2(lx2[0], lx2[1]);
-                l += lsum.x + lsum.y;
-                le += lxsum.x + lxsum.y;
+                if (!ok) break;
+                l += tile_l;
+                le += tile_le;
                 if (!prev_done) {
                     if (!wait_all(B.o_done + 8 * i, (t - 1) & 1)) { ok = false; break; }
                     ptx::tc_fence_after();

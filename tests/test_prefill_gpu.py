@@ -91,6 +91,28 @@ def test_prefill_large_scores_rescale():
     _check_rows(batch, out, lse, what="large scores")
 
 
+def _scale_keys(batch, b, lo, hi, factor):
+    """Multiply the K rows of keys [lo, hi) of request b by `factor`."""
+    k = syn.bf16_to_float(batch.kv_pool)
+    P = batch.page_size
+    for t in range(lo, min(hi, int(batch.kv_lens[b]))):
+        page = batch.page_table[batch.kv_indptr[b] + t // P]
+        k[page, 0, :, t % P, :] *= factor
+    batch.kv_pool = syn.bf16_bits(k)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_prefill_max_jumps_past_sum_limit(causal):
+    """Later key tiles score far above the first tile (by more than 64 in
+    log2 units), so a tile's P row sum passes the limit and the running max
+    is raised mid-item, O rescaled and the tile recomputed -- twice."""
+    batch = syn.make_batch("jump", [700], [700], 4, 1, 64, 16, causal=causal, seed=12)
+    _scale_keys(batch, 0, 300, 500, 30.0)
+    _scale_keys(batch, 0, 500, 700, 80.0)
+    out, lse, _ = run_prefill(batch)
+    _check_rows(batch, out, lse, what=f"max jump causal={causal}")
+
+
 def test_gptoss_prefill_full_sampled():
     batch = syn.gptoss_prefill(0)
     out, lse, plan = run_prefill(batch)
