@@ -67,12 +67,25 @@ struct PrefillCfg {
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kQBufs * 2 * kTile;
     static constexpr int kOffV = kOffK + kStagesK * kTile;
-    static constexpr int kOffBar = kOffV + kStagesV * kTile;
-    static constexpr int kNumBars = 2 * kQBufs + 2 * kStagesK + 2 * kStagesV + 8 + 2;
+    // At D = 64, P is split by keys: keys 0..63 go to TMEM (PV as TS MMA),
+    // keys 64..127 to shared memory (SS MMA), and the PV B operand is V
+    // extended by a ones column, so the same MMA also accumulates the row sum
+    // of the bf16-rounded P next to O (N = D + 16 costs no tensor time over
+    // N = D here).
+    static constexpr bool kSplitP = (D == 64);
+    static constexpr int kON = kSplitP ? D + 16 : D;      // O accumulator columns
+    static constexpr int kOffPb = kOffV + kStagesV * kTile;                 // per head 128 rows x 128 B
+    static constexpr int kOffOnes = kOffPb + (kSplitP ? 2 * kAtom : 0);     // 16 key rows x 128 B
+    static constexpr int kOffBar = kOffOnes + (kSplitP ? 2048 : 0);
+    static constexpr int kNumBars = 2 * kQBufs + 2 * kStagesK + 2 * kStagesV + 8 + 2 + 8;
     static constexpr int kSmem = 1024 + kOffBar + kNumBars * 8 + 16;
     static constexpr uint32_t kTmemCols = 512;
-    static constexpr uint32_t kColS = 0, kColO = 256, kColP = kSeparateP ? 384 : 0;
-    static constexpr uint32_t kStrideP = kSeparateP ? 64 : 128;
+    // TMEM columns of head slot i (every region starts on a multiple of 32).
+    // D = 64:  S 0 | 128, O (+ row sum) 256 | 384, P keys 0..63 at 352 | 480.
+    // D = 128: S 0 | 128, O 256 | 384, P aliases the first half of S.
+    static __device__ __forceinline__ uint32_t col_s(int i) { return i * 128; }
+    static __device__ __forceinline__ uint32_t col_o(int i) { return 256 + i * 128; }
+    static __device__ __forceinline__ uint32_t col_p(int i) { return kSplitP ? 256 + i * 128 + 96 : i * 128; }
 };
 
 struct PrefillArgs {
@@ -89,7 +102,7 @@ struct PrefillArgs {
 
 struct Bars {
     uint32_t q_full, q_empty, k_full, k_empty, v_full, v_empty, s_full, s_free, p_full, o_done,
-        v_aux, drain;
+        v_aux, drain, turn;
 };
 
 // Warp-uniform bounded wait.
@@ -123,6 +136,7 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
     B.o_done = B.p_full + 16;
     B.v_aux = B.o_done + 16;
     B.drain = B.v_aux + 8;
+    B.turn = B.drain + 8;   // [quadrant][head slot]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int item_begin = a.item_off[blockIdx.x], item_end = a.item_off[blockIdx.x + 1];
@@ -150,6 +164,7 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
         }
         ptx::mbar_init(B.v_aux, 1);
         ptx::mbar_init(B.drain, 2);
+        for (int k = 0; k < 8; ++k) ptx::mbar_init(B.turn + 8 * k, 1);
         *abort_flag = 0;
         ptx::prefetch_tmap(&q_map);
         ptx::prefetch_tmap(&kv_map);
@@ -158,6 +173,17 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::kTmemCols);
         ptx::tmem_relinquish();
+    }
+    if (C::kSplitP && warp == 2) {
+        // The ones block of the PV B operand: 16 key rows x 64 N values, N
+        // value 0 (the row-sum column) = 1.0 bf16, laid out with the same
+        // 128-byte swizzle as V (16-byte chunk c of row k sits at c ^ (k % 8)).
+        for (int idx = lane; idx < 2048 / 16; idx += 32) {
+            const int k = idx >> 3, c = idx & 7;
+            *reinterpret_cast<uint4*>(smem + C::kOffOnes + idx * 16) =
+                make_uint4(c == (k & 7) ? 0x3F80u : 0u, 0u, 0u, 0u);
+        }
+        ptx::fence_proxy_async_smem();
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -283,19 +309,26 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
         }
     } else if (warp == 1 || warp == 2) {
         // ================================================================ MMA issuers
-        // One issuing thread per head slot, so neither head's MMAs wait behind
-        // the other head's softmax.  Both release the shared K, V and Q stages.
-        if (lane == 0) {
-            const int i = warp - 1;
-            constexpr uint32_t idesc_qk = ptx::idesc_bf16(128, 128, false, false);
-            constexpr uint32_t idesc_pv = ptx::idesc_bf16(128, D, false, true);
-            const uint32_t t_s = tmem + C::kColS + i * 128;
-            const uint32_t t_o = tmem + C::kColO + i * D;
-            const uint32_t t_p = tmem + C::kColP + i * C::kStrideP;
-            int jg = 0, n_item = 0, hj = 0;
-            bool ok = true;
+        // One warp per head slot, so neither head's MMAs wait behind the other
+        // head's softmax.  The whole warp walks the schedule (descriptors and
+        // TMEM addresses stay warp-uniform, in uniform registers) and one
+        // elected lane issues each group of tcgen05.mma and commits.  Both
+        // warps release the shared K, V and Q stages.
+        const int i = __shfl_sync(0xffffffffu, warp - 1, 0);
+        constexpr uint32_t idesc_qk = ptx::idesc_bf16(128, 128, false, false);
+        constexpr uint32_t idesc_pv = ptx::idesc_bf16(128, C::kON, false, true);
+        const uint32_t t_s = tmem + C::col_s(i);
+        const uint32_t t_o = tmem + C::col_o(i);
+        const uint32_t t_p = tmem + C::col_p(i);
+        const bool leader = ptx::elect_one();
+        int jg = 0, n_item = 0, hj = 0;
+        bool ok = true;
 
-            auto qk = [&](int qb, int ks) {
+        // S = Q K^T of the K stage ks, then free the stage (and Q after the
+        // item's last QK^T).
+        auto qk = [&](int qb, int ks, bool last_of_item) {
+            if (leader) {
+                ptx::tc_fence_after();
                 const uint32_t qa = sbase + C::kOffQ + (qb * 2 + i) * C::kTile;
                 const uint32_t kb = sbase + C::kOffK + ks * C::kTile;
 #pragma unroll
@@ -305,83 +338,97 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                                    ptx::smem_desc_sw128(kb + off, 16, 1024), idesc_qk, kk > 0);
                 }
                 ptx::tc_commit(B.s_full + 8 * i);
-            };
-            auto pv = [&](int vs, bool first) {
+                ptx::tc_commit(B.k_empty + 8 * ks);
+                if (last_of_item) ptx::tc_commit(B.q_empty + 8 * qb);
+            }
+            __syncwarp();
+        };
+        // O += P V of the V stage vs, then free the stage.
+        auto pv = [&](int vs, bool first) {
+            if (leader) {
+                ptx::tc_fence_after();
                 const uint32_t vb = sbase + C::kOffV + vs * C::kTile;
+                if constexpr (C::kSplitP) {
+                    // B = [V | ones]: the second 64-wide N atom of every K step
+                    // is the same 16-row ones block (its own LBO per step).
+                    const uint32_t ones = sbase + C::kOffOnes;
+                    const uint32_t pb = sbase + C::kOffPb + i * C::kAtom;
 #pragma unroll
-                for (int kk = 0; kk < kPrefillKeys / 16; ++kk)
-                    ptx::tc_mma_ts(t_o, t_p + kk * 8, ptx::smem_desc_sw128(vb + kk * 2048, C::kAtom, 1024),
-                                   idesc_pv, (!first || kk > 0) ? 1u : 0u);
-                ptx::tc_commit(B.o_done + 8 * i);
-            };
-            auto kfull = [&](int t) { return ptx::mbar_wait(B.k_full + 8 * (t % C::kStagesK), (t / C::kStagesK) & 1); };
-            auto vfull = [&](int t) { return ptx::mbar_wait(B.v_full + 8 * (t % C::kStagesV), (t / C::kStagesV) & 1); };
-
-            for (int item = item_begin; ok && item < item_end; ++item, ++n_item) {
-                if (*abort_flag) { ok = false; break; }
-                const PrefillItem it = a.items[item];
-                const int n = it.n_kv_tiles;
-                const int qb = n_item % C::kQBufs;
-                if (!ptx::mbar_wait(B.q_full + 8 * qb, (n_item / C::kQBufs) & 1)) { ok = false; break; }
-                if (i >= it.n_heads) {
-                    // This head slot has no work in the item: only keep the
-                    // shared stages' arrival counts (after each stage is loaded).
-                    for (int j = 0; j < n && ok; ++j) {
-                        const int t = jg + j;
-                        if (!kfull(t)) { ok = false; break; }
-                        ptx::mbar_arrive(B.k_empty + 8 * (t % C::kStagesK));
-                        if (!vfull(t)) { ok = false; break; }
-                        ptx::mbar_arrive(B.v_empty + 8 * (t % C::kStagesV));
-                    }
-                    ptx::mbar_arrive(B.q_empty + 8 * qb);
-                    jg += n;
-                    continue;
-                }
-                if (C::kSeparateP) {
-                    // QK^T of tile j+1 is issued before PV of tile j.
-                    if (!kfull(jg)) { ok = false; break; }
-                    if (hj > 0 && !ptx::mbar_wait(B.s_free + 8 * i, (hj - 1) & 1)) { ok = false; break; }
-                    ptx::tc_fence_after();
-                    qk(qb, jg % C::kStagesK);
-                    ptx::tc_commit(B.k_empty + 8 * (jg % C::kStagesK));
-                    if (n == 1) ptx::tc_commit(B.q_empty + 8 * qb);
-                    for (int j = 0; j < n; ++j) {
-                        const int t = jg + j;
-                        if (j + 1 < n) {
-                            if (!kfull(t + 1) || !ptx::mbar_wait(B.s_free + 8 * i, (hj + j) & 1)) { ok = false; break; }
-                            ptx::tc_fence_after();
-                            qk(qb, (t + 1) % C::kStagesK);
-                            ptx::tc_commit(B.k_empty + 8 * ((t + 1) % C::kStagesK));
-                            if (j + 2 == n) ptx::tc_commit(B.q_empty + 8 * qb);
-                        }
-                        if (!vfull(t) || !ptx::mbar_wait(B.p_full + 8 * i, (hj + j) & 1)) { ok = false; break; }
-                        ptx::tc_fence_after();
-                        pv(t % C::kStagesV, j == 0);
-                        ptx::tc_commit(B.v_empty + 8 * (t % C::kStagesV));
+                    for (int kk = 0; kk < kPrefillKeys / 16; ++kk) {
+                        const uint32_t vk = vb + kk * 2048;
+                        const uint64_t bd = ptx::smem_desc_sw128(vk, ones - vk, 1024);
+                        if (kk < 4)
+                            ptx::tc_mma_ts(t_o, t_p + kk * 8, bd, idesc_pv, (!first || kk > 0) ? 1u : 0u);
+                        else
+                            ptx::tc_mma_ss(t_o, ptx::smem_desc_sw128(pb + (kk - 4) * 32, 16, 1024), bd, idesc_pv, 1u);
                     }
                 } else {
-                    // P aliases S: QK^T of tile j waits for PV of tile j-1.
-                    for (int j = 0; j < n; ++j) {
-                        const int t = jg + j;
-                        if (!kfull(t)) { ok = false; break; }
-                        if (hj + j > 0 && !ptx::mbar_wait(B.o_done + 8 * i, (hj + j - 1) & 1)) { ok = false; break; }
-                        ptx::tc_fence_after();
-                        qk(qb, t % C::kStagesK);
-                        ptx::tc_commit(B.k_empty + 8 * (t % C::kStagesK));
-                        if (j + 1 == n) ptx::tc_commit(B.q_empty + 8 * qb);
-                        if (!vfull(t) || !ptx::mbar_wait(B.p_full + 8 * i, (hj + j) & 1)) { ok = false; break; }
-                        ptx::tc_fence_after();
-                        pv(t % C::kStagesV, j == 0);
-                        ptx::tc_commit(B.v_empty + 8 * (t % C::kStagesV));
-                    }
+#pragma unroll
+                    for (int kk = 0; kk < kPrefillKeys / 16; ++kk)
+                        ptx::tc_mma_ts(t_o, t_p + kk * 8, ptx::smem_desc_sw128(vb + kk * 2048, C::kAtom, 1024),
+                                       idesc_pv, (!first || kk > 0) ? 1u : 0u);
                 }
-                jg += n;
-                hj += n;
+                ptx::tc_commit(B.o_done + 8 * i);
+                ptx::tc_commit(B.v_empty + 8 * vs);
             }
-            if (!ok) fail(ATTN_DEVICE_ERR_TIMEOUT);
-            // Arrives once every MMA this thread issued has finished.
-            ptx::tc_commit(B.drain);
+            __syncwarp();
+        };
+        auto kfull = [&](int t) { return wait_all(B.k_full + 8 * (t % C::kStagesK), (t / C::kStagesK) & 1); };
+        auto vfull = [&](int t) { return wait_all(B.v_full + 8 * (t % C::kStagesV), (t / C::kStagesV) & 1); };
+
+        for (int item = item_begin; ok && item < item_end; ++item, ++n_item) {
+            if (*abort_flag) { ok = false; break; }
+            const PrefillItem it = a.items[item];
+            const int n = it.n_kv_tiles;
+            const int qb = n_item % C::kQBufs;
+            if (!wait_all(B.q_full + 8 * qb, (n_item / C::kQBufs) & 1)) { ok = false; break; }
+            if (i >= it.n_heads) {
+                // This head slot has no work in the item: only keep the
+                // shared stages' arrival counts (after each stage is loaded).
+                for (int j = 0; j < n && ok; ++j) {
+                    const int t = jg + j;
+                    if (!kfull(t)) { ok = false; break; }
+                    if (leader) ptx::mbar_arrive(B.k_empty + 8 * (t % C::kStagesK));
+                    if (!vfull(t)) { ok = false; break; }
+                    if (leader) ptx::mbar_arrive(B.v_empty + 8 * (t % C::kStagesV));
+                }
+                if (leader) ptx::mbar_arrive(B.q_empty + 8 * qb);
+                __syncwarp();
+                jg += n;
+                continue;
+            }
+            if (C::kSeparateP) {
+                // QK^T of tile j+1 is issued before PV of tile j.
+                if (!kfull(jg)) { ok = false; break; }
+                if (hj > 0 && !wait_all(B.s_free + 8 * i, (hj - 1) & 1)) { ok = false; break; }
+                qk(qb, jg % C::kStagesK, n == 1);
+                for (int j = 0; j < n; ++j) {
+                    const int t = jg + j;
+                    if (j + 1 < n) {
+                        if (!kfull(t + 1) || !wait_all(B.s_free + 8 * i, (hj + j) & 1)) { ok = false; break; }
+                        qk(qb, (t + 1) % C::kStagesK, j + 2 == n);
+                    }
+                    if (!vfull(t) || !wait_all(B.p_full + 8 * i, (hj + j) & 1)) { ok = false; break; }
+                    pv(t % C::kStagesV, j == 0);
+                }
+            } else {
+                // P aliases S: QK^T of tile j waits for PV of tile j-1.
+                for (int j = 0; j < n; ++j) {
+                    const int t = jg + j;
+                    if (!kfull(t)) { ok = false; break; }
+                    if (hj + j > 0 && !wait_all(B.o_done + 8 * i, (hj + j - 1) & 1)) { ok = false; break; }
+                    qk(qb, t % C::kStagesK, j + 1 == n);
+                    if (!vfull(t) || !wait_all(B.p_full + 8 * i, (hj + j) & 1)) { ok = false; break; }
+                    pv(t % C::kStagesV, j == 0);
+                }
+            }
+            jg += n;
+            hj += n;
         }
+        if (!ok && leader) fail(ATTN_DEVICE_ERR_TIMEOUT);
+        // Arrives once every MMA this warp issued has finished.
+        if (leader) ptx::tc_commit(B.drain);
+        __syncwarp();
     } else if (warp >= 4) {
         // ================================================================ softmax
         ptx::setmaxnreg_inc<C::kRegsSoftmax>();
@@ -389,12 +436,23 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
         const int quad = warp & 3;                         // TMEM lane quadrant of this warp
         const int r = quad * 32 + lane;                    // row within the tile
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-        const uint32_t t_s = tmem + lane_off + C::kColS + i * 128;
-        const uint32_t t_o = tmem + lane_off + C::kColO + i * D;
-        const uint32_t t_p = tmem + lane_off + C::kColP + i * C::kStrideP;
+        const uint32_t t_s = tmem + lane_off + C::col_s(i);
+        const uint32_t t_o = tmem + lane_off + C::col_o(i);
+        const uint32_t t_p = tmem + lane_off + C::col_p(i);
+        // This thread's row of P keys 64..127 in shared memory (D = 64): 128
+        // bytes, 16-byte chunks swizzled by the row (K-major SW128 A operand).
+        const uint32_t pb_row = sbase + C::kOffPb + i * C::kAtom + (r >> 3) * 1024 + (r & 7) * 128;
         const float sl2 = a.scale_log2;
         int hj = 0;
         bool ok = true;
+        // Turn-taking with the other head slot's warp on the same SM
+        // sub-partition (same quadrant): in items with two heads the two warps
+        // run their exp loops one after the other, so each loop has the
+        // multi-function unit to itself while the other warp does its loads,
+        // waits and stores.  Head slot 0 goes first.
+        const uint32_t my_turn = B.turn + 8 * (quad * 2 + i), other_turn = B.turn + 8 * (quad * 2 + (i ^ 1));
+        int n_turn = 0;
+        if (i == 1 && lane == 0) ptx::mbar_arrive(other_turn);
         for (int item = item_begin; ok && item < item_end; ++item) {
             const PrefillItem it = a.items[item];
             if (i >= it.n_heads) continue;
@@ -402,6 +460,8 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
             const int n = it.n_kv_tiles;
             // l: row sum of the bf16-rounded P that the PV MMA consumes (it
             // normalises O); le: the same sum of the unrounded P (it gives lse).
+            // At D = 64 the keys' part of l accumulates in TMEM next to O (the
+            // ones column), and l here holds only the sink's term.
             float m_use = -INFINITY, l = 0.f, le = 0.f;
             if (a.sinks != nullptr) {
                 m_use = a.sinks[head] * kLog2e;
@@ -471,6 +531,8 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                 bool prev_done = !C::kSeparateP || t == 0;
                 uint32_t pk[2][32];
                 float tile_l = 0.f, tile_le = 0.f;
+                const bool take_turns = C::kSplitP && it.n_heads == 2;
+                if (take_turns && !wait_all(my_turn, n_turn & 1)) { ok = false; break; }
 #pragma unroll 1
                 for (int pass = 0;; ++pass) {
                     const float neg_m = m_use == -INFINITY ? 0.f : -m_use;
@@ -485,7 +547,8 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                                 ptx::fma2(make_float2(s[c * 64 + 2 * e], s[c * 64 + 2 * e + 1]), sl2x2, negm2);
                             const float2 p = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
                             pk[c][e] = ptx::pack_bf16x2(p.x, p.y);
-                            ls2[e & 1] = ptx::add2(ls2[e & 1], ptx::unpack_bf16x2(pk[c][e]));
+                            if constexpr (!C::kSplitP)
+                                ls2[e & 1] = ptx::add2(ls2[e & 1], ptx::unpack_bf16x2(pk[c][e]));
                             lx2[e & 1] = ptx::add2(lx2[e & 1], p);
                         }
                     }
@@ -508,6 +571,19 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                         for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
                         ptx::tmem_st32(t_o + c * 32, v);
                     }
+                    if constexpr (C::kSplitP) {   // the row-sum columns
+                        uint32_t v[16];
+                        ptx::tmem_ld16(t_o + D, v);
+                        ptx::tc_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                        ptx::tmem_st16(t_o + D, v);
+                    }
+                }
+                if (take_turns) {
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(other_turn);
+                    ++n_turn;
                 }
                 if (!ok) break;
                 l += tile_l;
@@ -517,7 +593,15 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                     ptx::tc_fence_after();
                 }
                 ptx::tmem_st32(t_p, pk[0]);
-                ptx::tmem_st32(t_p + 32, pk[1]);
+                if constexpr (C::kSplitP) {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        ptx::st_shared_v4(pb_row + ((c ^ (r & 7)) << 4), pk[1][4 * c], pk[1][4 * c + 1],
+                                          pk[1][4 * c + 2], pk[1][4 * c + 3]);
+                    ptx::fence_proxy_async_smem();   // the SS MMA reads it through the async proxy
+                } else {
+                    ptx::tmem_st32(t_p + 32, pk[1]);
+                }
                 ptx::tc_wait_st();
                 ptx::tc_fence_before();
                 __syncwarp();
@@ -528,6 +612,12 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
             if (!wait_all(B.o_done + 8 * i, (hj + n - 1) & 1)) { ok = false; break; }
             ptx::tc_fence_after();
             hj += n;
+            if constexpr (C::kSplitP) {
+                uint32_t v[16];
+                ptx::tmem_ld16(t_o + D, v);
+                ptx::tc_wait_ld();
+                l += __uint_as_float(v[0]);
+            }
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const bool store = r < it.n_rows;
             __nv_bfloat16* orow = a.out + ((size_t)(it.q_row0 + r) * a.Hq + head) * D;
