@@ -46,6 +46,12 @@ def _load():
             i64, p, p, i32, p, p]
         lib.oracle_merge_states.restype = None
         lib.oracle_merge_states.argtypes = [i64, i32, p, p, p, p, p, p]
+        lib.oracle_append_kv.restype = ctypes.c_int
+        lib.oracle_append_kv.argtypes = [i32, p, p, p, p, i32, i32, i32, i64, p, p, p]
+        for name in ("oracle_pack_heads", "oracle_unpack_heads"):
+            f = getattr(lib, name)
+            f.restype = ctypes.c_int
+            f.argtypes = [p, i64, i32, i32, i32, p, i64, i32, i32, p]
         _lib = lib
     return _lib
 
@@ -110,3 +116,42 @@ def merge_states(va, lsea, vb, lseb):
     lib.oracle_merge_states(n, D, _ptr(va), _ptr(lsea), _ptr(vb), _ptr(lseb), _ptr(vout),
                             _ptr(lseout))
     return vout, lseout
+
+
+def append_kv(batch, k_new, v_new):
+    """Return (pool after appending k_new / v_new [rows, Hkv, D] bf16 bits,
+    status); the batch's pool is not modified."""
+    lib = _load()
+    pool = np.array(batch.kv_pool, dtype=np.uint16, copy=True)
+    k_new = np.ascontiguousarray(k_new, dtype=np.uint16)
+    v_new = np.ascontiguousarray(v_new, dtype=np.uint16)
+    rc = lib.oracle_append_kv(batch.batch_size, _ptr(batch.qo_indptr), _ptr(batch.kv_indptr),
+                              _ptr(batch.page_table), _ptr(batch.last_page_len), batch.num_kv_heads,
+                              batch.head_dim, batch.page_size, batch.num_pages, _ptr(k_new),
+                              _ptr(v_new), _ptr(pool))
+    return pool, rc
+
+
+def pack_heads(pool, page_ids, h0, nh):
+    """Heads [h0, h0+nh) of the given pages of pool [pages, 2, Hkv, P, D] ->
+    (buf [n, 2, nh, P, D], status)."""
+    lib = _load()
+    pool = np.ascontiguousarray(pool, dtype=np.uint16)
+    ids = np.ascontiguousarray(page_ids, dtype=np.int32)
+    n_pages, _, Hkv, P, D = pool.shape
+    buf = np.zeros((len(ids), 2, nh, P, D), dtype=np.uint16)
+    rc = lib.oracle_pack_heads(_ptr(pool), n_pages, Hkv, P, D, _ptr(ids), len(ids), h0, nh, _ptr(buf))
+    return buf, rc
+
+
+def unpack_heads(pool, buf, page_ids, h0):
+    """Return (pool with buf [n, 2, nh, P, D] written into heads [h0, h0+nh)
+    of the given pages, status); the input pool is not modified."""
+    lib = _load()
+    out = np.array(pool, dtype=np.uint16, copy=True)
+    buf = np.ascontiguousarray(buf, dtype=np.uint16)
+    ids = np.ascontiguousarray(page_ids, dtype=np.int32)
+    n_pages, _, Hkv, P, D = out.shape
+    rc = lib.oracle_unpack_heads(_ptr(buf), n_pages, Hkv, P, D, _ptr(ids), len(ids), h0, buf.shape[2],
+                                 _ptr(out))
+    return out, rc

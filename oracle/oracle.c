@@ -236,3 +236,93 @@ void oracle_merge_states(int64_t n, int32_t D, const double* va, const double* l
         lseout[r] = L + log(wa + wb);
     }
 }
+
+/*
+ * KV append.  "Disaggregated prefill and decode" (Perplexity), section "KV
+ * Messenger": a layer's page copies start as soon as the model has finished
+ * appending the step's tokens to that layer's KV cache, and the cache entries
+ * are valid after the append and before attention.  The pages give no
+ * indexing; the reading taken here is that the qo_len tokens request b
+ * forwards are its newest cache positions, t = kv_len - qo_len + i for its
+ * i-th row (the same alignment as the causal mask), so row r = qo_indptr[b] + i
+ * of k_new / v_new ([rows][Hkv][D] bf16) goes to pool[page][0 / 1][g][t % P][:]
+ * with page = page_table[kv_indptr[b] + t / P].  Pure data movement: the bit
+ * patterns are copied unchanged.  A row whose page id lies outside
+ * [0, num_pages) is skipped and the return value is 1 (else 0).
+ */
+int oracle_append_kv(int32_t B, const int32_t* qo_indptr, const int32_t* kv_indptr,
+                     const int32_t* page_table, const int32_t* last_page_len, int32_t Hkv,
+                     int32_t D, int32_t P, int64_t num_pages, const uint16_t* k_new,
+                     const uint16_t* v_new, uint16_t* pool) {
+    int status = 0;
+    for (int32_t b = 0; b < B; ++b) {
+        int64_t kv_len = oracle_kv_len(kv_indptr, last_page_len, b, P);
+        int64_t qo_len = (int64_t)qo_indptr[b + 1] - qo_indptr[b];
+        for (int64_t i = 0; i < qo_len; ++i) {
+            int64_t t = kv_len - qo_len + i;
+            int64_t page = page_table[kv_indptr[b] + t / P];
+            if (page < 0 || page >= num_pages) {
+                status = 1;
+                continue;
+            }
+            int64_t r = qo_indptr[b] + i;
+            for (int32_t g = 0; g < Hkv; ++g) {
+                for (int kv = 0; kv < 2; ++kv) {
+                    const uint16_t* src = (kv == 0 ? k_new : v_new) + (r * Hkv + g) * (int64_t)D;
+                    uint16_t* dst = pool + (((page * 2 + kv) * Hkv + g) * P + t % P) * (int64_t)D;
+                    for (int32_t d = 0; d < D; ++d) dst[d] = src[d];
+                }
+            }
+        }
+    }
+    return status;
+}
+
+/*
+ * Head-slice pack and unpack of HND pages.  "Disaggregated prefill and
+ * decode", section "Sharded KV transfer": when the sending and receiving
+ * sides shard the KV cache over attention heads differently, pages are split
+ * or rebuilt from head slices, and the HND layout (heads before tokens) keeps
+ * a page's slice of heads contiguous so that it moves as one write.  Pack
+ * copies heads [h0, h0 + nh) of pages page_ids[0 .. n) out of the pool into
+ * buf[n][2][nh][P][D]; unpack writes such a buffer back into those heads of
+ * those pages.  Pages outside [0, num_pages) are skipped; the return value is
+ * then 1 (else 0).
+ */
+int oracle_pack_heads(const uint16_t* pool, int64_t num_pages, int32_t Hkv, int32_t P, int32_t D,
+                      const int32_t* page_ids, int64_t n, int32_t h0, int32_t nh, uint16_t* buf) {
+    int status = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t page = page_ids[i];
+        if (page < 0 || page >= num_pages) {
+            status = 1;
+            continue;
+        }
+        for (int kv = 0; kv < 2; ++kv)
+            for (int32_t h = 0; h < nh; ++h)
+                for (int32_t p = 0; p < P; ++p)
+                    for (int32_t d = 0; d < D; ++d)
+                        buf[(((i * 2 + kv) * nh + h) * P + p) * (int64_t)D + d] =
+                            pool[(((page * 2 + kv) * Hkv + h0 + h) * P + p) * (int64_t)D + d];
+    }
+    return status;
+}
+
+int oracle_unpack_heads(const uint16_t* buf, int64_t num_pages, int32_t Hkv, int32_t P, int32_t D,
+                        const int32_t* page_ids, int64_t n, int32_t h0, int32_t nh, uint16_t* pool) {
+    int status = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t page = page_ids[i];
+        if (page < 0 || page >= num_pages) {
+            status = 1;
+            continue;
+        }
+        for (int kv = 0; kv < 2; ++kv)
+            for (int32_t h = 0; h < nh; ++h)
+                for (int32_t p = 0; p < P; ++p)
+                    for (int32_t d = 0; d < D; ++d)
+                        pool[(((page * 2 + kv) * Hkv + h0 + h) * P + p) * (int64_t)D + d] =
+                            buf[(((i * 2 + kv) * nh + h) * P + p) * (int64_t)D + d];
+    }
+    return status;
+}

@@ -180,3 +180,12 @@ WORKLOADS = {
     "qwen_decode": qwen_decode,
     "mixed": mixed,
 }
+
+
+def new_kv_rows(batch: Batch, seed: int = 0):
+    """The step's new K and V rows, one per query row of the batch: bf16 bits
+    [rows, Hkv, D] each, ~N(0, 1), seeded (the input of the KV append)."""
+    rng = _rng(1000003 + seed)
+    n = batch.total_rows * batch.num_kv_heads * batch.head_dim
+    shape = (batch.total_rows, batch.num_kv_heads, batch.head_dim)
+    return _normal_bf16(rng, n).reshape(shape), _normal_bf16(rng, n).reshape(shape)

@@ -294,3 +294,122 @@ def test_request_without_queries_or_keys():
     a = _small_batch(12, [2, 0, 3], [5, 0, 7], Hq=2, Hkv=1, D=4, P=2)
     out, lse = oracle.sink_attention(a)
     assert out.shape[0] == 5 and np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
+
+
+# ---------------------------------------------------------------- KV append
+# "Disaggregated prefill and decode", section "KV Messenger": the step's new
+# tokens are appended to the KV cache before attention; the i-th forwarded row
+# of a request is its cache position kv_len - qo_len + i.
+
+def _literal_append_batch():
+    """Hand-made batch: P = 4, Hkv = 2, D = 2, 4 pages.  Request 0 owns pages
+    [3, 1] with 2 tokens on the last page (kv_len 6) and forwards 2 rows;
+    request 1 owns page [0] with 3 tokens (kv_len 3) and forwards 1 row."""
+    sentinel = np.uint16(0xAAAA)
+    pool = np.full((4, 2, 2, 4, 2), sentinel, dtype=np.uint16)
+    return syn.Batch(name="literal", num_qo_heads=2, num_kv_heads=2, head_dim=2, page_size=4, causal=True,
+                     sm_scale=1.0, qo_lens=np.array([2, 1]), kv_lens=np.array([6, 3]),
+                     qo_indptr=np.array([0, 2, 3], dtype=np.int32), kv_indptr=np.array([0, 2, 3], dtype=np.int32),
+                     page_table=np.array([3, 1, 0], dtype=np.int32), last_page_len=np.array([2, 3], dtype=np.int32),
+                     q=np.zeros((3, 2, 2), dtype=np.uint16), kv_pool=pool, sinks=None)
+
+
+def test_append_literal_positions():
+    b = _literal_append_batch()
+    k = np.array([[[100 * r + 10 * g + d for d in range(2)] for g in range(2)] for r in range(3)], dtype=np.uint16)
+    v = k + np.uint16(5000)
+    pool, rc = oracle.append_kv(b, k, v)
+    assert rc == 0
+    expected = b.kv_pool.copy()
+    # (row r, its page, row in page), listed by hand from the layout above:
+    # request 0 rows 0, 1 -> positions 4, 5 -> second page (id 1), rows 0, 1;
+    # request 1 row 2 -> position 2 -> page 0, row 2.
+    for r, page, slot in ((0, 1, 0), (1, 1, 1), (2, 0, 2)):
+        expected[page, 0, :, slot, :] = k[r]
+        expected[page, 1, :, slot, :] = v[r]
+    np.testing.assert_array_equal(pool, expected)
+    assert b.kv_pool[0, 0, 0, 0, 0] == 0xAAAA          # the input pool is untouched
+
+
+def test_append_then_attention_sees_new_rows_in_order():
+    """A fresh prefill (qo_len == kv_len): after the append, the oracle's
+    attention over the cache equals brute-force causal sink attention computed
+    directly on the new rows -- ties the append's positions to the page walk."""
+    batch = syn.make_batch("fresh", [5, 9], [5, 9], 4, 2, 8, 4, seed=21)
+    k_new, v_new = syn.new_kv_rows(batch, seed=3)
+    pool, rc = oracle.append_kv(batch, k_new, v_new)
+    assert rc == 0
+    batch.kv_pool = pool
+    out, lse = oracle.sink_attention(batch)
+    q = syn.bf16_to_float(batch.q).astype(np.float64)
+    kf = syn.bf16_to_float(k_new).astype(np.float64)
+    vf = syn.bf16_to_float(v_new).astype(np.float64)
+    G = batch.num_qo_heads // batch.num_kv_heads
+    for b in range(2):
+        r0, n = int(batch.qo_indptr[b]), int(batch.qo_lens[b])
+        for i in range(n):
+            for h in range(batch.num_qo_heads):
+                s = kf[r0:r0 + i + 1, h // G] @ q[r0 + i, h] * batch.sm_scale
+                w = np.exp(np.append(s, batch.sinks[h]) - max(s.max(), batch.sinks[h]))
+                ref = (w[:-1, None] * vf[r0:r0 + i + 1, h // G]).sum(0) / w.sum()
+                np.testing.assert_allclose(out[r0 + i, h], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_append_bad_page_is_skipped():
+    b = _literal_append_batch()
+    b.page_table = np.array([3, 7, 0], dtype=np.int32)      # page 7 is outside the 4-page pool
+    k = np.ones((3, 2, 2), dtype=np.uint16)
+    pool, rc = oracle.append_kv(b, k, k)
+    assert rc == 1
+    assert np.all(pool[0, :, :, 2, :] == 1)                  # request 1's row still lands
+    assert np.count_nonzero(pool != 0xAAAA) == 2 * 2 * 2     # and nothing else changed
+
+
+# ------------------------------------------------------ head-slice pack / unpack
+# "Disaggregated prefill and decode", section "Sharded KV transfer": HND keeps
+# a page's head slice contiguous, so head-sharded pages are split and rebuilt
+# from such slices.
+
+def test_pack_literal():
+    pool = np.arange(3 * 2 * 3 * 2 * 2, dtype=np.uint16).reshape(3, 2, 3, 2, 2)   # [pages, K/V, Hkv=3, P=2, D=2]
+    buf, rc = oracle.pack_heads(pool, [2, 0], 1, 2)
+    assert rc == 0
+    # buf[i, kv, h, p, d] = pool[page_i, kv, 1 + h, p, d], written out for page 2 then page 0
+    expected = np.stack([np.stack([pool[2, kv, 1:3] for kv in range(2)]),
+                         np.stack([pool[0, kv, 1:3] for kv in range(2)])])
+    np.testing.assert_array_equal(buf, expected)
+
+
+def test_pack_all_heads_is_a_page_gather():
+    rng = np.random.default_rng(5)
+    pool = rng.integers(0, 65535, size=(9, 2, 4, 16, 8), dtype=np.uint16)
+    ids = np.array([7, 2, 2, 0, 8], dtype=np.int32)
+    buf, rc = oracle.pack_heads(pool, ids, 0, 4)
+    assert rc == 0
+    np.testing.assert_array_equal(buf, pool[ids])
+
+
+def test_unpack_inverts_pack_and_touches_only_the_slice():
+    rng = np.random.default_rng(6)
+    pool = rng.integers(0, 65535, size=(6, 2, 4, 4, 8), dtype=np.uint16)
+    ids = np.array([5, 1, 3], dtype=np.int32)
+    buf, _ = oracle.pack_heads(pool, ids, 1, 2)
+    zero = np.zeros_like(pool)
+    rebuilt, rc = oracle.unpack_heads(zero, buf, ids, 1)
+    assert rc == 0
+    mask = np.zeros(pool.shape, dtype=bool)
+    mask[ids[:, None], :, 1:3] = True
+    np.testing.assert_array_equal(rebuilt[mask], pool[mask])
+    assert np.all(rebuilt[~mask] == 0)
+    # the two halves of a head-sharded page rebuild it exactly
+    lo, _ = oracle.pack_heads(pool, ids, 0, 2)
+    hi, _ = oracle.pack_heads(pool, ids, 2, 2)
+    full, _ = oracle.unpack_heads(zero, lo, ids, 0)
+    full, _ = oracle.unpack_heads(full, hi, ids, 2)
+    np.testing.assert_array_equal(full[ids], pool[ids])
+
+
+def test_pack_bad_page_is_skipped():
+    pool = np.ones((2, 2, 2, 2, 2), dtype=np.uint16)
+    buf, rc = oracle.pack_heads(pool, [1, -1], 0, 2)
+    assert rc == 1 and np.all(buf[0] == 1) and np.all(buf[1] == 0)
