@@ -70,7 +70,76 @@ def prefill_flops(batch):
 
 
 # ----------------------------------------------------------------- clocks
+class NvmlSampler:
+    """Samples the SM clock, its maximum, the board power and the active
+    clock-event reasons every few ms from a thread, through NVML (read-only
+    queries on the driver's libnvidia-ml), so that even a short timed region
+    gets samples.  Falls back to an nvidia-smi loop if NVML is unavailable."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, uuid: str, period_s: float = 0.002):
+        self.uuid, self.period = uuid, period_s
+        self.samples, self.thread, self.stop_flag = [], None, False
+        self.nvml = self.handle = None
+        self.fallback = None
+
+    def _open(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByUUID(self.uuid.encode(), ctypes.byref(h)) != 0:
+            raise RuntimeError("no NVML handle for " + self.uuid)
+        self.nvml, self.handle = lib, h
+        self.reason_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+
+    def _poll(self):
+        import ctypes
+        clk, mx, mw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stop_flag:
+            ok = (self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(clk)) == 0 and
+                  self.nvml.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(mx)) == 0)
+            if ok:
+                p = mw.value / 1000.0 if self.nvml.nvmlDeviceGetPowerUsage(self.handle, ctypes.byref(mw)) == 0 else None
+                r = rs.value if self.reason_fn(self.handle, ctypes.byref(rs)) == 0 else 0
+                self.samples.append((float(clk.value), float(mx.value), p, int(r)))
+            time.sleep(self.period)
+
+    def start(self):
+        import threading
+        try:
+            self._open()
+        except Exception:
+            self.fallback = ClockSampler(self.uuid)
+            self.fallback.start()
+            return
+        self.thread = threading.Thread(target=self._poll, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        if self.fallback is not None:
+            return self.fallback.stop()
+        self.stop_flag = True
+        self.thread.join(timeout=5)
+        try:
+            self.nvml.nvmlShutdown()
+        except Exception:
+            pass
+        sm = [x[0] for x in self.samples]
+        smax = [x[1] for x in self.samples]
+        pw = [x[2] for x in self.samples if x[2] is not None]
+        reasons = sorted({name for x in self.samples for bit, name in self.REASONS.items() if x[3] & bit})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "sm_min_mhz": min(sm) if sm else None, "power_w_median": statistics.median(pw) if pw else None,
+                "reasons": reasons, "samples": len(sm), "source": "nvml"}
+
+
 class ClockSampler:
+    """nvidia-smi loop (fallback sampler)."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -116,7 +185,7 @@ class ClockSampler:
         busy = [s for s in sm if smax and s > 0.5 * max(smax)] or sm
         return {"sm_mhz": statistics.median(busy) if busy else None,
                 "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "source": "nvidia-smi"}
 
 
 # -------------------------------------------------------------- distributed
@@ -261,7 +330,7 @@ def run_ours(args, world, rank, local):
     if plan.device_error():
         raise RuntimeError("decode kernel recorded a device error")
 
-    sampler = ClockSampler(gpu_id)
+    sampler = NvmlSampler(gpu_id)
     sampler.start()
     barrier(world)
     torch.cuda.synchronize()
@@ -346,6 +415,40 @@ def run_ours(args, world, rank, local):
                                     "peak_source": peak_src}}
             launches += psteps
 
+    # ---- KV-cache legs (HBM copies): the step's append on the prefill batch,
+    # and a head-slice pack of half the heads of every page of the decode pool.
+    kvcache = None
+    if not args.no_prefill and prefill is not None and "unavailable" not in prefill:
+        k_new, v_new = syn.new_kv_rows(pbatch, seed=rank)
+        kd = torch.from_numpy(k_new.view(np.int16)).view(torch.bfloat16).to(dev)
+        vd = torch.from_numpy(v_new.view(np.int16)).view(torch.bfloat16).to(dev)
+        app = lambda: pplan.append_kv(kd, vd, pkv)
+        for _ in range(args.warmup):
+            app()
+        asteps = max(3, args.steps // 10)
+        atimes = time_device(app, asteps, flush, stream)
+        amean = sum(atimes) / len(atimes) / 1e3
+        abytes = 2 * 2 * kd.numel() * 2                       # K and V rows, read once + written once
+        ids = torch.from_numpy(np.unique(batch.page_table)).to(dev)
+        nh = batch.num_kv_heads // 2
+        buf = torch.empty((ids.numel(), 2, nh, batch.page_size, batch.head_dim), dtype=torch.bfloat16, device=dev)
+        pk = lambda: binding.attn_pack_kv_heads(kv, ids, 0, nh, buf=buf)
+        for _ in range(args.warmup):
+            pk()
+        ktimes = time_device(pk, asteps, flush, stream)
+        kmean = sum(ktimes) / len(ktimes) / 1e3
+        kbytes = 2 * buf.numel() * 2                           # slice read once + buffer written once
+        peak = float(peaks["hbm_gbs"])
+        kvcache = {
+            "append": {"workload": "gptoss_prefill rows (new K/V of every query row)", "bytes": abytes,
+                       "us": amean * 1e6, "value": abytes / amean / 1e9, "unit": "GB/s",
+                       "frac_of_hbm_peak": abytes / amean / 1e9 / peak},
+            "pack_heads": {"workload": f"gptoss_decode pool, heads [0,{nh}) of {ids.numel()} pages",
+                           "bytes": kbytes, "us": kmean * 1e6, "value": kbytes / kmean / 1e9, "unit": "GB/s",
+                           "frac_of_hbm_peak": kbytes / kmean / 1e9 / peak},
+        }
+        launches += 2 * asteps
+
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -374,7 +477,7 @@ def run_ours(args, world, rank, local):
                        "parallelism": f"replicas x{world}", "plan_us": plan_us,
                        "decode_units": units},
             "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
-            "clocks": clocks, "cpu_baseline": cpu, "prefill": prefill,
+            "clocks": clocks, "cpu_baseline": cpu, "prefill": prefill, "kv_cache": kvcache,
         }
         print(json.dumps(line), flush=True)
 

@@ -208,6 +208,53 @@ ATTN_API attn_status attn_merge_states(const void* va, const float* lsea, const 
 ATTN_API attn_status attn_decode_noalloc(attn_plan_t plan, const void* q, const void* kv_cache,
                                          const float* sinks, void* out, float* lse, void* stream);
 
+/*
+ * attn_append_kv -- write the step's new K and V rows into the paged cache,
+ * the step that runs before attention ("Disaggregated prefill and decode"
+ * (Perplexity), section "KV Messenger": the model appends a layer's new tokens
+ * to its KV cache, and the entries are valid after that append and before
+ * attention).  Every query row of the plan is one new token: row i of request
+ * b is cache position t = kv_len - qo_len + i (kv_len as given to attn_plan,
+ * i.e. counting the new tokens), stored at page page_table[kv_indptr[b] + t/P],
+ * row t % P, so the pages must already be allocated in the plan's page table.
+ *
+ *   k_new, v_new  bf16 [total_qo_rows][Hkv][head_dim], device, 16-byte aligned
+ *   kv_cache      bf16 [num_pages][2][Hkv][page_size][head_dim] HND pool,
+ *                 device, 16-byte aligned; only the new tokens' rows change
+ * Bit-exact copy.  Needs a bound workspace.  Page ids outside [0, num_pages)
+ * set ATTN_DEVICE_ERR_PAGE_ID and that row is skipped.  Async on `stream`.
+ */
+ATTN_API attn_status attn_append_kv(attn_plan_t plan, const void* k_new, const void* v_new, void* kv_cache,
+                                    void* stream);
+
+/*
+ * attn_pack_kv_heads / attn_unpack_kv_heads -- move a head slice of HND pages
+ * to or from one contiguous buffer, the local half of a head-sharded KV
+ * transfer ("Disaggregated prefill and decode", section "Sharded KV transfer":
+ * pages are split or rebuilt from head slices when sender and receiver shard
+ * the cache over attention heads differently, and the HND layout keeps a
+ * page's head slice contiguous).  The network part is not in this library.
+ *
+ *   kv_cache      bf16 [num_pages][2][num_kv_heads][page_size][head_dim], device
+ *   page_ids      int32 [n_pages], device: pages to move, in buffer order
+ *   buf           bf16 [n_pages][2][n_heads][page_size][head_dim], device
+ *   heads         [head_begin, head_begin + n_heads) of num_kv_heads
+ *   device_error  optional device int32; ATTN_DEVICE_ERR_PAGE_ID is OR-ed in
+ *                 when a page id lies outside [0, num_pages) (that page is
+ *                 skipped).  NULL: such pages are skipped silently.
+ * Pack reads the pool and writes buf; unpack reads buf and writes only the
+ * slice's bytes of the listed pages.  head_dim a multiple of 8; kv_cache and
+ * buf 16-byte aligned.  Bit-exact copies.  Async on `stream`.
+ */
+ATTN_API attn_status attn_pack_kv_heads(const void* kv_cache, int64_t num_pages, int32_t num_kv_heads,
+                                        int32_t page_size, int32_t head_dim, const int32_t* page_ids,
+                                        int64_t n_pages, int32_t head_begin, int32_t n_heads, void* buf,
+                                        int32_t* device_error, void* stream);
+ATTN_API attn_status attn_unpack_kv_heads(const void* buf, int64_t num_pages, int32_t num_kv_heads,
+                                          int32_t page_size, int32_t head_dim, const int32_t* page_ids,
+                                          int64_t n_pages, int32_t head_begin, int32_t n_heads, void* kv_cache,
+                                          int32_t* device_error, void* stream);
+
 /* Copy the plan's summary into *info (host only). */
 ATTN_API attn_status attn_plan_get_info(attn_plan_t plan, attn_plan_info* info);
 

@@ -7,7 +7,7 @@ machines without the built library; any use of the API without the library
 raises immediately -- there is no CPU fallback.
 """
 _API = ("Plan", "attn_plan", "attn_prefill", "attn_decode", "attn_merge_states",
-        "load_library", "library_path", "AttnError")
+        "attn_pack_kv_heads", "attn_unpack_kv_heads", "load_library", "library_path", "AttnError")
 
 
 def __getattr__(name):

@@ -55,6 +55,9 @@ def _declare(lib):
         "attn_prefill": (st, [p, p, p, p, p, p, p]),
         "attn_decode_noalloc": (st, [p, p, p, p, p, p, p]),
         "attn_merge_states": (st, [p, p, p, p, p, p, i32, i32, i32, p]),
+        "attn_append_kv": (st, [p, p, p, p, p]),
+        "attn_pack_kv_heads": (st, [p, i64, i32, i32, i32, p, i64, i32, i32, p, p, p]),
+        "attn_unpack_kv_heads": (st, [p, i64, i32, i32, i32, p, i64, i32, i32, p, p, p]),
         "attn_plan_get_info": (st, [p, p]),
         "attn_plan_get_decode_units": (st, [p, p, i64]),
         "attn_plan_get_prefill_items": (st, [p, p, i64]),
@@ -216,6 +219,21 @@ class Plan:
         out = torch.empty_like(q) if out is None else out
         return self._launch("attn_prefill", q, kv_cache, sinks, out, lse, stream)
 
+    def append_kv(self, k_new, v_new, kv_cache, stream=None):
+        """Write the new K/V rows ([rows, Hkv, D] bf16, one per query row) into
+        their cache positions in kv_cache (in place)."""
+        shape = (self.total_rows, self.num_kv_heads, self.head_dim)
+        for name, t in (("k_new", k_new), ("v_new", v_new), ("kv_cache", kv_cache)):
+            if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous()):
+                raise TypeError(f"{name} must be a contiguous bfloat16 CUDA tensor")
+        if tuple(k_new.shape) != shape or tuple(v_new.shape) != shape:
+            raise ValueError(f"k_new / v_new must be {list(shape)}")
+        if tuple(kv_cache.shape) != (self.num_pages, 2, self.num_kv_heads, self.page_size, self.head_dim):
+            raise ValueError("kv_cache must be [num_pages, 2, Hkv, page_size, head_dim]")
+        _check("attn_append_kv", load_library().attn_append_kv(
+            self._handle, _ptr(k_new), _ptr(v_new), _ptr(kv_cache), _stream_ptr(stream)))
+        return kv_cache
+
 
 def attn_plan(qo_indptr, kv_indptr, page_table, last_page_len, num_qo_heads, num_kv_heads,
               head_dim, page_size, causal=True, sm_scale=None, num_pages=None, num_sms=0,
@@ -247,3 +265,37 @@ def attn_merge_states(va, lsea, vb, lseb, vout=None, lseout=None, stream=None):
         _ptr(va), _ptr(lsea), _ptr(vb), _ptr(lseb), _ptr(vout), _ptr(lseout), n, H, D,
         _stream_ptr(stream)))
     return vout, lseout
+
+
+def _head_slice(fn_name, kv_cache, page_ids, head_begin, n_heads, buf, device_error, stream):
+    for name, t in (("kv_cache", kv_cache), ("buf", buf)):
+        if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous()):
+            raise TypeError(f"{name} must be a contiguous bfloat16 CUDA tensor")
+    if not (isinstance(page_ids, torch.Tensor) and page_ids.is_cuda and page_ids.dtype == torch.int32
+            and page_ids.is_contiguous()):
+        raise TypeError("page_ids must be a contiguous int32 CUDA tensor")
+    num_pages, two, hkv, P, D = kv_cache.shape
+    if two != 2 or tuple(buf.shape) != (page_ids.numel(), 2, n_heads, P, D):
+        raise ValueError("buf must be [n_pages, 2, n_heads, page_size, head_dim] for the pool's page shape")
+    _check(fn_name, getattr(load_library(), fn_name)(
+        _ptr(kv_cache) if fn_name == "attn_pack_kv_heads" else _ptr(buf), num_pages, hkv, P, D, _ptr(page_ids),
+        page_ids.numel(), head_begin, n_heads,
+        _ptr(buf) if fn_name == "attn_pack_kv_heads" else _ptr(kv_cache), _ptr(device_error),
+        _stream_ptr(stream)))
+
+
+def attn_pack_kv_heads(kv_cache, page_ids, head_begin, n_heads, buf=None, device_error=None, stream=None):
+    """Heads [head_begin, head_begin + n_heads) of pages page_ids of the HND
+    pool -> buf [n_pages, 2, n_heads, page_size, head_dim]."""
+    if buf is None:
+        buf = torch.empty((page_ids.numel(), 2, n_heads, kv_cache.shape[3], kv_cache.shape[4]),
+                          dtype=kv_cache.dtype, device=kv_cache.device)
+    _head_slice("attn_pack_kv_heads", kv_cache, page_ids, head_begin, n_heads, buf, device_error, stream)
+    return buf
+
+
+def attn_unpack_kv_heads(buf, page_ids, head_begin, kv_cache, device_error=None, stream=None):
+    """Write buf [n_pages, 2, n_heads, page_size, head_dim] into heads
+    [head_begin, head_begin + n_heads) of pages page_ids of the pool (in place)."""
+    _head_slice("attn_unpack_kv_heads", kv_cache, page_ids, head_begin, buf.shape[2], buf, device_error, stream)
+    return kv_cache

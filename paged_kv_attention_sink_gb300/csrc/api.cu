@@ -89,6 +89,10 @@ extern "C" attn_status attn_plan_bind_workspace(attn_plan_t plan, void* workspac
          cudaMemcpyAsync(ws + L.item_off, plan->item_off.data(), plan->item_off.size() * sizeof(int32_t),
                          cudaMemcpyHostToDevice, s) != cudaSuccess))
         return ATTN_ERR_CUDA;
+    if (!plan->append_slots.empty() &&
+        cudaMemcpyAsync(ws + L.append, plan->append_slots.data(), plan->append_slots.size() * sizeof(int32_t),
+                        cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return ATTN_ERR_CUDA;
     // counters and the error word are adjacent: clear both.
     if (cudaMemsetAsync(ws + L.counters, 0, L.part_lse - L.counters, s) != cudaSuccess) return ATTN_ERR_CUDA;
     plan->ws = ws;
@@ -141,6 +145,50 @@ extern "C" attn_status attn_merge_states(const void* va, const float* lsea, cons
         return ATTN_ERR_INVALID_ARG;
     return attn::launch_merge_states(va, lsea, vb, lseb, vout, lseout, (int64_t)n_tokens * n_heads,
                                      head_dim, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" attn_status attn_append_kv(attn_plan_t plan, const void* k_new, const void* v_new, void* kv_cache,
+                                     void* stream) {
+    if (!plan) return ATTN_ERR_INVALID_ARG;
+    if (!plan->bound) return ATTN_ERR_NOT_BOUND;
+    if (plan->info.total_qo_rows == 0) return ATTN_OK;
+    if (!k_new || !v_new || !kv_cache) return ATTN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new) |
+         reinterpret_cast<uintptr_t>(kv_cache)) & 15)
+        return ATTN_ERR_INVALID_ARG;
+    return attn::launch_append_kv(plan, k_new, v_new, kv_cache, static_cast<cudaStream_t>(stream));
+}
+
+namespace {
+attn_status head_slice(bool unpack, void* kv_cache, int64_t num_pages, int32_t num_kv_heads, int32_t page_size,
+                       int32_t head_dim, const int32_t* page_ids, int64_t n_pages, int32_t head_begin,
+                       int32_t n_heads, void* buf, int32_t* device_error, void* stream) {
+    if (n_pages < 0 || num_pages <= 0 || num_kv_heads <= 0 || page_size <= 0 || head_dim <= 0 ||
+        head_dim % 8 != 0 || head_begin < 0 || n_heads <= 0 || head_begin + n_heads > num_kv_heads)
+        return ATTN_ERR_INVALID_ARG;
+    if (n_pages == 0) return ATTN_OK;
+    if (!kv_cache || !buf || !page_ids) return ATTN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(kv_cache) | reinterpret_cast<uintptr_t>(buf)) & 15)
+        return ATTN_ERR_INVALID_ARG;
+    return attn::launch_head_slice(unpack, kv_cache, buf, page_ids, n_pages, num_pages, num_kv_heads, page_size,
+                                   head_dim, head_begin, n_heads, device_error, static_cast<cudaStream_t>(stream));
+}
+}  // namespace
+
+extern "C" attn_status attn_pack_kv_heads(const void* kv_cache, int64_t num_pages, int32_t num_kv_heads,
+                                         int32_t page_size, int32_t head_dim, const int32_t* page_ids,
+                                         int64_t n_pages, int32_t head_begin, int32_t n_heads, void* buf,
+                                         int32_t* device_error, void* stream) {
+    return head_slice(false, const_cast<void*>(kv_cache), num_pages, num_kv_heads, page_size, head_dim, page_ids,
+                      n_pages, head_begin, n_heads, buf, device_error, stream);
+}
+
+extern "C" attn_status attn_unpack_kv_heads(const void* buf, int64_t num_pages, int32_t num_kv_heads,
+                                           int32_t page_size, int32_t head_dim, const int32_t* page_ids,
+                                           int64_t n_pages, int32_t head_begin, int32_t n_heads, void* kv_cache,
+                                           int32_t* device_error, void* stream) {
+    return head_slice(true, kv_cache, num_pages, num_kv_heads, page_size, head_dim, page_ids, n_pages, head_begin,
+                      n_heads, const_cast<void*>(buf), device_error, stream);
 }
 
 extern "C" attn_status attn_plan_device_error(attn_plan_t plan, int32_t* code, void* stream) {

@@ -55,7 +55,8 @@ struct PrefillItem {
 static_assert(sizeof(PrefillItem) == 48, "prefill item is 12 int32");
 
 struct WorkspaceLayout {
-    size_t units = 0, items = 0, item_off = 0, counters = 0, err = 0, part_lse = 0, part_o = 0, total = 0;
+    size_t units = 0, items = 0, item_off = 0, append = 0, counters = 0, err = 0, part_lse = 0, part_o = 0,
+           total = 0;
 };
 
 // CTAs of the decode kernel resident per SM for a head dim (matches its
@@ -73,6 +74,7 @@ struct attn_plan_s {
 
     std::vector<attn::DecodeUnit> units;
     std::vector<attn::PrefillItem> items;
+    std::vector<int32_t> append_slots;    // per query row: page-table slot, row in page
     std::vector<int32_t> item_off;        // CTA c runs items [item_off[c], item_off[c+1])
     int32_t prefill_ctas = 0;
     int32_t n_groups = 0;

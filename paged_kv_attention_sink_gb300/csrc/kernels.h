@@ -15,6 +15,13 @@ attn_status launch_prefill(attn_plan_s* plan, const void* q_map, const void* kv_
 attn_status launch_merge_states(const void* va, const float* lsea, const void* vb,
                                 const float* lseb, void* vout, float* lseout, int64_t rows,
                                 int head_dim, cudaStream_t stream);
+// New K/V rows of the plan's query rows into their HND page slots.
+attn_status launch_append_kv(attn_plan_s* plan, const void* k_new, const void* v_new, void* kv_cache,
+                             cudaStream_t stream);
+// Heads [h0, h0 + nh) of pages page_ids[0..n) <-> buf[n][2][nh][P][D].
+attn_status launch_head_slice(bool unpack, void* kv_cache, void* buf, const int32_t* page_ids, int64_t n,
+                              int64_t num_pages, int32_t Hkv, int32_t P, int32_t D, int32_t h0, int32_t nh,
+                              int32_t* err, cudaStream_t stream);
 
 }  // namespace attn
 

@@ -202,11 +202,24 @@ extern "C" attn_status attn_plan(const int32_t* qo_indptr, const int32_t* kv_ind
         plan->prefill_ctas = ctas;
     }
 
+    // ---- KV append: cache position of every query row (the row's token is
+    // appended at t = kv_len - qo_len + i): page-table slot and row in page.
+    plan->append_slots.resize((size_t)total_rows * 2);
+    for (int32_t b = 0; b < batch; ++b) {
+        for (int64_t i = 0; i < qo_len[b]; ++i) {
+            const int64_t t = kv_len[b] - qo_len[b] + i;
+            const int64_t r = qo_indptr[b] + i;
+            plan->append_slots[2 * r] = (int32_t)(kv_indptr[b] + t / page_size);
+            plan->append_slots[2 * r + 1] = (int32_t)(t % page_size);
+        }
+    }
+
     // ---- workspace layout (every region 256-byte aligned).
     WorkspaceLayout& L = plan->layout;
     size_t off = 0;
     L.units = off;    off = align_up(off + plan->units.size() * sizeof(DecodeUnit), 256);
     L.items = off;    off = align_up(off + plan->items.size() * sizeof(PrefillItem), 256);
+    L.append = off;   off = align_up(off + plan->append_slots.size() * sizeof(int32_t), 256);
     L.item_off = off; off = align_up(off + plan->item_off.size() * sizeof(int32_t), 256);
     L.counters = off; off = align_up(off + (size_t)plan->n_groups * sizeof(int32_t), 256);
     L.err = off;      off = align_up(off + sizeof(int32_t), 256);

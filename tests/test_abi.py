@@ -205,3 +205,19 @@ def test_merge_states_argument_checks(lib):
     assert lib.attn_merge_states(p, p, p, p, p, None, 4, 2, 6, None) == INVALID   # D % 4
     assert lib.attn_merge_states(p, p, p, p, p, None, -1, 2, 8, None) == INVALID
     assert lib.attn_merge_states(None, None, None, None, None, None, 0, 2, 8, None) == OK
+
+
+def test_head_slice_argument_checks(lib):
+    p = ctypes.c_void_p(0x10000)
+    # head range outside the pool's heads, head_dim not a multiple of 8, misaligned pointers
+    assert lib.attn_pack_kv_heads(p, 10, 8, 16, 64, p, 4, 6, 4, p, None, None) == INVALID
+    assert lib.attn_pack_kv_heads(p, 10, 8, 16, 60, p, 4, 0, 4, p, None, None) == INVALID
+    assert lib.attn_unpack_kv_heads(ctypes.c_void_p(0x10008), 10, 8, 16, 64, p, 4, 0, 4, p, None, None) == INVALID
+    assert lib.attn_pack_kv_heads(p, 10, 8, 16, 64, p, 0, 0, 4, p, None, None) == OK      # nothing to move
+
+
+def test_append_requires_bound_workspace(lib):
+    st, h, _ = plan(lib, [1], [1], [4])
+    dummy = ctypes.c_void_p(0x10000)
+    assert lib.attn_append_kv(h, dummy, dummy, dummy, None) == 5     # not bound
+    lib.attn_plan_destroy(h)
