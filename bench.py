@@ -415,6 +415,32 @@ def run_ours(args, world, rank, local):
                                     "peak_source": peak_src}}
             launches += psteps
 
+    # ---- ragged (non-paged) prefill on the same batch: contiguous K / V
+    ragged = None
+    if not args.no_prefill and prefill is not None and "unavailable" not in prefill:
+        P = pbatch.page_size
+        ks, vs = [], []
+        for b in range(pbatch.batch_size):
+            t = np.arange(int(pbatch.kv_lens[b]))
+            pages = pbatch.page_table[pbatch.kv_indptr[b] + t // P]
+            ks.append(pbatch.kv_pool[pages, 0, :, t % P, :])
+            vs.append(pbatch.kv_pool[pages, 1, :, t % P, :])
+        rk = torch.from_numpy(np.concatenate(ks).view(np.int16)).view(torch.bfloat16).to(dev)
+        rv = torch.from_numpy(np.concatenate(vs).view(np.int16)).view(torch.bfloat16).to(dev)
+        rplan = binding.RaggedPlan(pbatch.qo_indptr, np.concatenate([[0], np.cumsum(pbatch.kv_lens)]),
+                                   pbatch.num_qo_heads, pbatch.num_kv_heads, pbatch.head_dim,
+                                   causal=pbatch.causal, sm_scale=pbatch.sm_scale, device=dev)
+        rag = lambda: rplan.prefill(pq, rk, rv, psk, pout, plse)
+        for _ in range(args.warmup):
+            rag()
+        rsteps = max(3, args.steps // 10)
+        rtimes = time_device(rag, rsteps, flush, stream)
+        rmean = sum(rtimes) / len(rtimes) / 1e3
+        rtf = prefill_flops(pbatch) / rmean / 1e12
+        ragged = {"workload": "gptoss_prefill, contiguous K/V (no cache)", "value": rtf, "unit": "TFLOP/s",
+                  "ms_per_step": rmean * 1e3, "frac_of_bf16_peak": rtf / float(peaks["bf16_tflops"])}
+        launches += rsteps
+
     # ---- KV-cache legs (HBM copies): the step's append on the prefill batch,
     # and a head-slice pack of half the heads of every page of the decode pool.
     kvcache = None
@@ -477,7 +503,7 @@ def run_ours(args, world, rank, local):
                        "parallelism": f"replicas x{world}", "plan_us": plan_us,
                        "decode_units": units},
             "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
-            "clocks": clocks, "cpu_baseline": cpu, "prefill": prefill, "kv_cache": kvcache,
+            "clocks": clocks, "cpu_baseline": cpu, "prefill": prefill, "prefill_ragged": ragged, "kv_cache": kvcache,
         }
         print(json.dumps(line), flush=True)
 

@@ -163,6 +163,31 @@ ATTN_API attn_status attn_prefill(attn_plan_t plan, const void* q, const void* k
                          const float* sinks, void* out, float* lse, void* stream);
 
 /*
+ * attn_plan_ragged / attn_prefill_ragged -- the same sink attention over
+ * contiguous, unpadded K and V with no KV cache, for embedding-style serving
+ * ("Fast embeddings on GPUs" (Perplexity), section "ROSE": with no KV cache
+ * the attention kernels take ragged inputs so that nothing is padded).
+ *
+ *   qo_indptr  host int32 [batch + 1]: request b's query rows
+ *   kv_indptr  host int32 [batch + 1]: request b's rows of k and v (tokens,
+ *              not pages); qo_len <= kv_len, queries aligned to the end of
+ *              the keys for the causal mask as in attn_plan
+ *   q, out     bf16 [qo_indptr[batch]][Hq][head_dim]
+ *   k, v       bf16 [kv_indptr[batch]][Hkv][head_dim] (16-byte aligned)
+ *   sinks, lse as in attn_prefill
+ * Every request (qo_len = 1 included) runs on the tcgen05 prefill kernel; the
+ * plan has no decode work (attn_decode on it does nothing) and cannot be used
+ * with attn_prefill or attn_append_kv (ATTN_ERR_INVALID_ARG).  Workspace and
+ * error word as for attn_plan.
+ */
+ATTN_API attn_status attn_plan_ragged(const int32_t* qo_indptr, const int32_t* kv_indptr, int32_t batch,
+                                      int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                                      int32_t causal, float sm_scale, int32_t num_sms, attn_plan_t* plan_out,
+                                      size_t* workspace_bytes_out);
+ATTN_API attn_status attn_prefill_ragged(attn_plan_t plan, const void* q, const void* k, const void* v,
+                                         const float* sinks, void* out, float* lse, void* stream);
+
+/*
  * attn_merge_states -- combine two attention states over disjoint key sets
  * into the state over their union, by the log-sum-exp rule implied by the
  * split along the KV length in "GPT-OSS on day 0", section "Sink Attention"

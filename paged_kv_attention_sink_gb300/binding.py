@@ -56,6 +56,8 @@ def _declare(lib):
         "attn_decode_noalloc": (st, [p, p, p, p, p, p, p]),
         "attn_merge_states": (st, [p, p, p, p, p, p, i32, i32, i32, p]),
         "attn_append_kv": (st, [p, p, p, p, p]),
+        "attn_plan_ragged": (st, [p, p, i32, i32, i32, i32, i32, f32, i32, p, p]),
+        "attn_prefill_ragged": (st, [p, p, p, p, p, p, p, p]),
         "attn_pack_kv_heads": (st, [p, i64, i32, i32, i32, p, i64, i32, i32, p, p, p]),
         "attn_unpack_kv_heads": (st, [p, i64, i32, i32, i32, p, i64, i32, i32, p, p, p]),
         "attn_plan_get_info": (st, [p, p]),
@@ -233,6 +235,61 @@ class Plan:
         _check("attn_append_kv", load_library().attn_append_kv(
             self._handle, _ptr(k_new), _ptr(v_new), _ptr(kv_cache), _stream_ptr(stream)))
         return kv_cache
+
+
+class RaggedPlan(Plan):
+    """A planned batch over contiguous K / V (no KV cache): every request runs
+    on the prefill kernel.  qo_indptr, kv_indptr: host int arrays (token CSR)."""
+
+    def __init__(self, qo_indptr, kv_indptr, num_qo_heads: int, num_kv_heads: int, head_dim: int,
+                 causal: bool = True, sm_scale: Optional[float] = None, num_sms: int = 0, device="cuda",
+                 stream=None):
+        lib = load_library()
+        self._handle = None
+        qo = _i32_host(qo_indptr)
+        kv = _i32_host(kv_indptr)
+        self.batch = len(qo) - 1
+        self.num_qo_heads, self.num_kv_heads, self.head_dim = num_qo_heads, num_kv_heads, head_dim
+        self.causal = bool(causal)
+        self.sm_scale = float(sm_scale) if sm_scale is not None else head_dim ** -0.5
+        self.total_rows = int(qo[-1]) if len(qo) else 0
+        self.kv_tokens = int(kv[-1]) if len(kv) else 0
+        handle = ctypes.c_void_p()
+        ws_bytes = ctypes.c_size_t()
+        _check("attn_plan_ragged", lib.attn_plan_ragged(
+            qo.ctypes.data_as(ctypes.c_void_p), kv.ctypes.data_as(ctypes.c_void_p), self.batch, num_qo_heads,
+            num_kv_heads, head_dim, int(self.causal), self.sm_scale, int(num_sms), ctypes.byref(handle),
+            ctypes.byref(ws_bytes)))
+        self._handle = handle
+        self.workspace = torch.empty(max(int(ws_bytes.value), 256), dtype=torch.uint8, device=device)
+        _check("attn_plan_bind_workspace", lib.attn_plan_bind_workspace(
+            self._handle, _ptr(self.workspace), self.workspace.numel(), _stream_ptr(stream)))
+
+    def prefill(self, q, k, v, sinks=None, out=None, lse=None, stream=None):
+        H, Hkv, D = self.num_qo_heads, self.num_kv_heads, self.head_dim
+        out = torch.empty_like(q) if out is None else out
+        for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+            if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous()):
+                raise TypeError(f"{name} must be a contiguous bfloat16 CUDA tensor")
+        if tuple(q.shape) != (self.total_rows, H, D) or tuple(out.shape) != (self.total_rows, H, D):
+            raise ValueError(f"q / out must be [{self.total_rows}, {H}, {D}]")
+        if tuple(k.shape) != (self.kv_tokens, Hkv, D) or tuple(v.shape) != (self.kv_tokens, Hkv, D):
+            raise ValueError(f"k / v must be [{self.kv_tokens}, {Hkv}, {D}]")
+        if sinks is not None and not (sinks.is_cuda and sinks.dtype == torch.float32 and
+                                      sinks.is_contiguous() and sinks.numel() == H):
+            raise TypeError("sinks must be a contiguous float32 CUDA tensor of num_qo_heads values")
+        if lse is not None and not (lse.is_cuda and lse.dtype == torch.float32 and lse.is_contiguous()
+                                    and tuple(lse.shape) == (self.total_rows, H)):
+            raise TypeError("lse must be a contiguous float32 CUDA tensor [rows, Hq]")
+        _check("attn_prefill_ragged", load_library().attn_prefill_ragged(
+            self._handle, _ptr(q), _ptr(k), _ptr(v), _ptr(sinks), _ptr(out), _ptr(lse), _stream_ptr(stream)))
+        return out, lse
+
+    def decode(self, *args, **kwargs):
+        raise TypeError("a ragged plan has no KV cache; use prefill(q, k, v, ...)")
+
+    def append_kv(self, *args, **kwargs):
+        raise TypeError("a ragged plan has no KV cache")
 
 
 def attn_plan(qo_indptr, kv_indptr, page_table, last_page_len, num_qo_heads, num_kv_heads,

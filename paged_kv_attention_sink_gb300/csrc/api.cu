@@ -43,6 +43,22 @@ bool make_kv_map(void* map, const void* kv, const attn_plan_s* p, int box_rows) 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Contiguous K or V [tokens][Hkv][D] (ragged plans) as a 3-D tensor
+// {dim, KV head, token}: one box is 128 tokens x 64 dims of one KV head,
+// stored like a 128-row page box; rows past the end read as zero.
+bool make_ragged_map(void* map, const void* x, const attn_plan_s* p) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)p->D, (cuuint64_t)p->Hkv, (cuuint64_t)p->kv_tokens};
+    cuuint64_t strides[2] = {(cuuint64_t)p->D * 2, (cuuint64_t)p->Hkv * p->D * 2};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)attn::kPrefillKeys};
+    cuuint32_t elem[3] = {1, 1, 1};
+    return fn(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+              const_cast<void*>(x), dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // q [rows][Hq][D] as a 3-D tensor {dim, head, row}: one box is 128 rows x 64
 // dims of one head; rows past the end read as zero.
 bool make_q_map(void* map, const void* q, const attn_plan_s* p) {
@@ -116,6 +132,7 @@ extern "C" attn_status attn_decode(attn_plan_t plan, const void* q, const void* 
 
 extern "C" attn_status attn_prefill(attn_plan_t plan, const void* q, const void* kv_cache,
                                     const float* sinks, void* out, float* lse, void* stream) {
+    if (plan && plan->ragged) return ATTN_ERR_INVALID_ARG;   // attn_prefill_ragged
     if (plan && plan->bound && plan->items.empty()) return ATTN_OK;
     attn_status st = check_launch(plan, q, kv_cache, out);
     if (st != ATTN_OK) return st;
@@ -128,8 +145,32 @@ extern "C" attn_status attn_prefill(attn_plan_t plan, const void* q, const void*
         if (!make_q_map(plan->q_map_prefill, q, plan)) return ATTN_ERR_CUDA;
         plan->q_map_prefill_ptr = q;
     }
-    return attn::launch_prefill(plan, plan->q_map_prefill, plan->kv_map_prefill, sinks, out, lse,
+    return attn::launch_prefill(plan, plan->q_map_prefill, plan->kv_map_prefill, nullptr, sinks, out, lse,
                                 static_cast<cudaStream_t>(stream));
+}
+
+extern "C" attn_status attn_prefill_ragged(attn_plan_t plan, const void* q, const void* k, const void* v,
+                                           const float* sinks, void* out, float* lse, void* stream) {
+    if (!plan) return ATTN_ERR_INVALID_ARG;
+    if (!plan->ragged) return ATTN_ERR_INVALID_ARG;   // paged plans go through attn_prefill
+    if (plan->bound && plan->items.empty()) return ATTN_OK;
+    attn_status st = check_launch(plan, q, k, out);
+    if (st != ATTN_OK) return st;
+    if (!v || !aligned16(v)) return ATTN_ERR_INVALID_ARG;
+    if (plan->kv_map_prefill_ptr != k) {
+        if (!make_ragged_map(plan->kv_map_prefill, k, plan)) return ATTN_ERR_CUDA;
+        plan->kv_map_prefill_ptr = k;
+    }
+    if (plan->v_map_prefill_ptr != v) {
+        if (!make_ragged_map(plan->v_map_prefill, v, plan)) return ATTN_ERR_CUDA;
+        plan->v_map_prefill_ptr = v;
+    }
+    if (plan->q_map_prefill_ptr != q) {
+        if (!make_q_map(plan->q_map_prefill, q, plan)) return ATTN_ERR_CUDA;
+        plan->q_map_prefill_ptr = q;
+    }
+    return attn::launch_prefill(plan, plan->q_map_prefill, plan->kv_map_prefill, plan->v_map_prefill, sinks, out,
+                                lse, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" attn_status attn_merge_states(const void* va, const float* lsea, const void* vb,
@@ -149,7 +190,7 @@ extern "C" attn_status attn_merge_states(const void* va, const float* lsea, cons
 
 extern "C" attn_status attn_append_kv(attn_plan_t plan, const void* k_new, const void* v_new, void* kv_cache,
                                      void* stream) {
-    if (!plan) return ATTN_ERR_INVALID_ARG;
+    if (!plan || plan->ragged) return ATTN_ERR_INVALID_ARG;   // a ragged plan has no cache
     if (!plan->bound) return ATTN_ERR_NOT_BOUND;
     if (plan->info.total_qo_rows == 0) return ATTN_OK;
     if (!k_new || !v_new || !kv_cache) return ATTN_ERR_INVALID_ARG;

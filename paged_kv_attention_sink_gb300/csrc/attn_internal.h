@@ -71,6 +71,8 @@ struct attn_plan_s {
     int32_t num_pages = 0;
     int32_t num_sms = 0;
     const int32_t* page_table = nullptr;  // device, borrowed
+    bool ragged = false;                  // contiguous K / V (attn_plan_ragged), no page table
+    int64_t kv_tokens = 0;                // ragged: rows of K and V (kv_indptr[batch])
 
     std::vector<attn::DecodeUnit> units;
     std::vector<attn::PrefillItem> items;
@@ -93,4 +95,6 @@ struct attn_plan_s {
     const void* kv_map_prefill_ptr = nullptr;
     alignas(64) unsigned char q_map_prefill[128];
     const void* q_map_prefill_ptr = nullptr;
+    alignas(64) unsigned char v_map_prefill[128];   // ragged: K in kv_map_prefill, V here
+    const void* v_map_prefill_ptr = nullptr;
 };

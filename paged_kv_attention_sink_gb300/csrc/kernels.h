@@ -10,7 +10,8 @@ namespace attn {
 // kv_map / q_map point at CUtensorMap objects built by the API layer.
 attn_status launch_decode(attn_plan_s* plan, const void* q, const void* kv_map, const float* sinks,
                           void* out, float* lse, cudaStream_t stream);
-attn_status launch_prefill(attn_plan_s* plan, const void* q_map, const void* kv_map,
+// v_map: the V tensor map of a ragged plan (NULL for a paged plan).
+attn_status launch_prefill(attn_plan_s* plan, const void* q_map, const void* kv_map, const void* v_map,
                            const float* sinks, void* out, float* lse, cudaStream_t stream);
 attn_status launch_merge_states(const void* va, const float* lsea, const void* vb,
                                 const float* lseb, void* vout, float* lseout, int64_t rows,

@@ -24,15 +24,21 @@ bool supported_page_size(int p) { return p == 16 || p == 32 || p == 64 || p == 1
 
 }  // namespace
 
-extern "C" attn_status attn_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
-                                 const int32_t* page_table, const int32_t* last_page_len,
-                                 int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads,
-                                 int32_t head_dim, int32_t page_size, int32_t causal,
-                                 float sm_scale, int32_t num_pages_in_pool, int32_t num_sms,
-                                 attn_plan_t* plan_out, size_t* workspace_bytes_out) {
+namespace {
+
+// Shared planner.  Paged: kv_indptr is the page CSR into page_table, kv_len
+// comes from the page count and last_page_len.  Ragged: kv_indptr is the token
+// CSR into contiguous K / V arrays, every request becomes prefill work items
+// (there is no cache to split decode over), and page_table / last_page_len /
+// num_pages_in_pool are unused.
+attn_status make_plan(bool ragged, const int32_t* qo_indptr, const int32_t* kv_indptr,
+                      const int32_t* page_table, const int32_t* last_page_len, int32_t batch,
+                      int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                      int32_t causal, float sm_scale, int32_t num_pages_in_pool, int32_t num_sms,
+                      attn_plan_t* plan_out, size_t* workspace_bytes_out) {
     using namespace attn;
     if (!plan_out || !workspace_bytes_out || batch < 0) return ATTN_ERR_INVALID_ARG;
-    if (batch > 0 && (!qo_indptr || !kv_indptr || !last_page_len)) return ATTN_ERR_INVALID_ARG;
+    if (batch > 0 && (!qo_indptr || !kv_indptr || (!ragged && !last_page_len))) return ATTN_ERR_INVALID_ARG;
     if (num_qo_heads <= 0 || num_kv_heads <= 0 || num_qo_heads % num_kv_heads != 0)
         return ATTN_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
@@ -49,7 +55,10 @@ extern "C" attn_status attn_plan(const int32_t* qo_indptr, const int32_t* kv_ind
         int64_t np = (int64_t)kv_indptr[b + 1] - kv_indptr[b];
         if (nq < 0 || np < 0) return ATTN_ERR_INVALID_ARG;
         int64_t kv = 0;
-        if (np > 0) {
+        if (ragged) {
+            kv = np;   // tokens
+            np = 0;
+        } else if (np > 0) {
             if (last_page_len[b] < 1 || last_page_len[b] > page_size) return ATTN_ERR_INVALID_ARG;
             kv = (np - 1) * page_size + last_page_len[b];
         }
@@ -84,6 +93,8 @@ extern "C" attn_status attn_plan(const int32_t* qo_indptr, const int32_t* kv_ind
     plan->num_pages = num_pages_in_pool;
     plan->num_sms = num_sms;
     plan->page_table = page_table;
+    plan->ragged = ragged;
+    plan->kv_tokens = (ragged && batch > 0) ? kv_indptr[batch] : 0;
 
     const int G = num_qo_heads / num_kv_heads;
     const int n_slices = (G + kMaxSliceHeads - 1) / kMaxSliceHeads;
@@ -93,11 +104,11 @@ extern "C" attn_status attn_plan(const int32_t* qo_indptr, const int32_t* kv_ind
     int32_t n_decode = 0, n_prefill = 0;
     int64_t decode_tokens = 0, prefill_pairs = 0;
     for (int32_t b = 0; b < batch; ++b) {
-        if (qo_len[b] == 1) {
+        if (qo_len[b] == 1 && !ragged) {
             ++n_decode;
             decode_tokens += kv_len[b];
             total_blocks += (kv_len[b] + kBlockTokens - 1) / kBlockTokens * num_kv_heads * n_slices;
-        } else if (qo_len[b] > 1) {
+        } else if (qo_len[b] > 1 || (ragged && qo_len[b] == 1)) {
             ++n_prefill;
         }
     }
@@ -107,7 +118,7 @@ extern "C" attn_status attn_plan(const int32_t* qo_indptr, const int32_t* kv_ind
     chunk = std::min<int64_t>(std::max<int64_t>(chunk, kDecodeMinChunkBlocks), kDecodeMaxChunkBlocks);
 
     for (int32_t b = 0; b < batch; ++b) {
-        if (qo_len[b] != 1) continue;
+        if (qo_len[b] != 1 || ragged) continue;
         const int64_t nblk = (kv_len[b] + kBlockTokens - 1) / kBlockTokens;
         int64_t n_chunks = std::max<int64_t>(1, (nblk + chunk / 2) / chunk);
         n_chunks = std::max<int64_t>(n_chunks, (nblk + kDecodeMaxChunkBlocks - 1) / kDecodeMaxChunkBlocks);
@@ -146,7 +157,7 @@ extern "C" attn_status attn_plan(const int32_t* qo_indptr, const int32_t* kv_ind
     // ---- prefill: one item per (128-row tile, pair of query heads of a group),
     // visiting 128-key KV tiles up to the causal diagonal.
     for (int32_t b = 0; b < batch; ++b) {
-        if (qo_len[b] <= 1) continue;
+        if (qo_len[b] == 0 || (qo_len[b] == 1 && !ragged)) continue;
         const int64_t prefix = kv_len[b] - qo_len[b];
         for (int64_t r = 0; r < qo_len[b]; ++r)
             prefill_pairs += causal ? (prefix + r + 1) : kv_len[b];
@@ -204,8 +215,8 @@ extern "C" attn_status attn_plan(const int32_t* qo_indptr, const int32_t* kv_ind
 
     // ---- KV append: cache position of every query row (the row's token is
     // appended at t = kv_len - qo_len + i): page-table slot and row in page.
-    plan->append_slots.resize((size_t)total_rows * 2);
-    for (int32_t b = 0; b < batch; ++b) {
+    plan->append_slots.resize(ragged ? 0 : (size_t)total_rows * 2);
+    for (int32_t b = 0; b < batch && !ragged; ++b) {
         for (int64_t i = 0; i < qo_len[b]; ++i) {
             const int64_t t = kv_len[b] - qo_len[b] + i;
             const int64_t r = qo_indptr[b] + i;
@@ -245,6 +256,27 @@ extern "C" attn_status attn_plan(const int32_t* qo_indptr, const int32_t* kv_ind
     *plan_out = plan;
     *workspace_bytes_out = L.total;
     return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" attn_status attn_plan(const int32_t* qo_indptr, const int32_t* kv_indptr,
+                                 const int32_t* page_table, const int32_t* last_page_len,
+                                 int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads,
+                                 int32_t head_dim, int32_t page_size, int32_t causal,
+                                 float sm_scale, int32_t num_pages_in_pool, int32_t num_sms,
+                                 attn_plan_t* plan_out, size_t* workspace_bytes_out) {
+    return make_plan(false, qo_indptr, kv_indptr, page_table, last_page_len, batch, num_qo_heads, num_kv_heads,
+                     head_dim, page_size, causal, sm_scale, num_pages_in_pool, num_sms, plan_out,
+                     workspace_bytes_out);
+}
+
+extern "C" attn_status attn_plan_ragged(const int32_t* qo_indptr, const int32_t* kv_indptr, int32_t batch,
+                                        int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                                        int32_t causal, float sm_scale, int32_t num_sms, attn_plan_t* plan_out,
+                                        size_t* workspace_bytes_out) {
+    return make_plan(true, qo_indptr, kv_indptr, nullptr, nullptr, batch, num_qo_heads, num_kv_heads, head_dim,
+                     attn::kPrefillKeys, causal, sm_scale, 0, num_sms, plan_out, workspace_bytes_out);
 }
 
 extern "C" attn_status attn_plan_get_info(attn_plan_t plan, attn_plan_info* info) {

@@ -110,10 +110,14 @@ __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity) {
     return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity));
 }
 
-template <int D>
+// kRagged: K and V are contiguous [tokens][Hkv][D] arrays (kv_map over K,
+// v_map over V) instead of the paged HND pool (kv_map; v_map unused), and an
+// item's page_base is its first token.
+template <int D, bool kRagged>
 __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
 prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
-                         const __grid_constant__ CUtensorMap kv_map, const PrefillArgs a) {
+                         const __grid_constant__ CUtensorMap kv_map,
+                         const __grid_constant__ CUtensorMap v_map, const PrefillArgs a) {
     using C = PrefillCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -219,6 +223,7 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
             return (min(kPrefillKeys, x.kv_len - j * kPrefillKeys) + P - 1) / P;
         };
         auto load_pages = [&](const PrefillItem& x, int j) {
+            if constexpr (kRagged) return 0;
             return lane < n_load_of(x, j) ? a.page_table[x.page_base + j * pages_per_tile + lane] : -1;
         };
         int item = item_begin, j = 0;
@@ -252,10 +257,12 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
             }
             const int valid = min(kPrefillKeys, it.kv_len - j * kPrefillKeys);
             const int n_load = (valid + P - 1) / P;
-            const bool bad = lane < n_load && (page < 0 || page >= a.num_pages);
+            const bool bad = !kRagged && lane < n_load && (page < 0 || page >= a.num_pages);
             const unsigned bad_mask = __ballot_sync(0xffffffffu, bad);
             if (bad_mask && lane == 0) atomicOr(a.err, ATTN_DEVICE_ERR_PAGE_ID);
-            const int tx = (n_load - __popc(bad_mask)) * box_bytes * (D / 64);
+            // Ragged: one box of 128 tokens per 64 dims (rows past the request
+            // or the array arrive too, and are masked or zeroed like a page tail).
+            const int tx = kRagged ? C::kTile : (n_load - __popc(bad_mask)) * box_bytes * (D / 64);
 
             const int st = jg % n_stages;
             if (jg >= n_stages && !wait_all(empty0 + 8 * st, ((jg / n_stages) - 1) & 1)) {
@@ -270,10 +277,16 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
             if (lane == 0) ptx::mbar_arrive_expect_tx(bar, tx);
             // One page box per lane: the boxes of a tile leave in one warp instruction.
             __syncwarp();
-            if (lane < n_load && page >= 0 && page < a.num_pages)
+            if constexpr (kRagged) {
+                if (lane == 0)
+                    for (int c = 0; c < D / 64; ++c)
+                        ptx::tma_load_3d_hint(dst0 + st * C::kTile + c * C::kAtom, is_k ? &kv_map : &v_map, bar,
+                                              c * 64, it.kv_head, it.page_base + j * kPrefillKeys, policy);
+            } else if (lane < n_load && page >= 0 && page < a.num_pages) {
                 for (int c = 0; c < D / 64; ++c)
                     ptx::tma_load_3d_hint(dst0 + st * C::kTile + c * C::kAtom + lane * box_bytes, &kv_map, bar,
                                           c * 64, 0, (page * 2 + (is_k ? 0 : 1)) * a.Hkv + it.kv_head, policy);
+            }
             if (ragged) {
                 // Only an item's last tile can be ragged: wait for its rows,
                 // zero V rows [valid, 128) (they may hold anything), publish.
@@ -657,11 +670,11 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
     }
 }
 
-template <int D>
-cudaError_t launch(const CUtensorMap& qm, const CUtensorMap& km, const PrefillArgs& args, int grid,
-                   cudaStream_t stream) {
+template <int D, bool kRagged>
+cudaError_t launch(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm, const PrefillArgs& args,
+                   int grid, cudaStream_t stream) {
     using C = PrefillCfg<D>;
-    auto kernel = prefill_sink_attn_kernel<D>;
+    auto kernel = prefill_sink_attn_kernel<D, kRagged>;
     static bool configured = false;
     if (!configured) {
         cudaFuncAttributes fa;
@@ -673,13 +686,13 @@ cudaError_t launch(const CUtensorMap& qm, const CUtensorMap& km, const PrefillAr
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    kernel<<<grid, C::kThreads, C::kSmem, stream>>>(qm, km, args);
+    kernel<<<grid, C::kThreads, C::kSmem, stream>>>(qm, km, vm, args);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-attn_status launch_prefill(attn_plan_s* plan, const void* q_map, const void* kv_map,
+attn_status launch_prefill(attn_plan_s* plan, const void* q_map, const void* kv_map, const void* v_map,
                            const float* sinks, void* out, float* lse, cudaStream_t stream) {
     if (plan->items.empty()) return ATTN_OK;
     PrefillArgs a;
@@ -698,10 +711,16 @@ attn_status launch_prefill(attn_plan_s* plan, const void* q_map, const void* kv_
     a.scale_log2 = plan->sm_scale * kLog2e;
     const CUtensorMap& qm = *static_cast<const CUtensorMap*>(q_map);
     const CUtensorMap& km = *static_cast<const CUtensorMap*>(kv_map);
+    const CUtensorMap& vm = *static_cast<const CUtensorMap*>(v_map ? v_map : kv_map);
     // Persistent grid: one CTA per planned item list (at most one per SM; the
     // kernel holds all of an SM's TMEM).
     const int grid = plan->prefill_ctas;
-    const cudaError_t e = plan->D == 64 ? launch<64>(qm, km, a, grid, stream) : launch<128>(qm, km, a, grid, stream);
+    cudaError_t e;
+    if (plan->ragged)
+        e = plan->D == 64 ? launch<64, true>(qm, km, vm, a, grid, stream) : launch<128, true>(qm, km, vm, a, grid, stream);
+    else
+        e = plan->D == 64 ? launch<64, false>(qm, km, vm, a, grid, stream)
+                          : launch<128, false>(qm, km, vm, a, grid, stream);
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

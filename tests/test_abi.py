@@ -221,3 +221,25 @@ def test_append_requires_bound_workspace(lib):
     dummy = ctypes.c_void_p(0x10000)
     assert lib.attn_append_kv(h, dummy, dummy, dummy, None) == 5     # not bound
     lib.attn_plan_destroy(h)
+
+
+def test_ragged_plan_covers_every_request(lib):
+    qo = np.array([0, 1, 301, 301, 350], dtype=np.int32)        # a 1-row request and an empty one
+    kv = np.array([0, 9, 309, 320, 369], dtype=np.int32)        # token CSR
+    handle = ctypes.c_void_p()
+    ws = ctypes.c_size_t()
+    st = lib.attn_plan_ragged(qo.ctypes.data_as(ctypes.c_void_p), kv.ctypes.data_as(ctypes.c_void_p), 4, 8, 2,
+                              64, 1, 0.125, 152, ctypes.byref(handle), ctypes.byref(ws))
+    assert st == OK
+    info, u, it = units_of(lib, handle)
+    assert info.num_decode_units == 0 and info.num_prefill_requests == 3
+    rows = set()
+    for (row0, nrows, kv_off, kv_len, pos0, g, head0, nh, ntiles, key_end, _, _) in it:
+        b = int(np.searchsorted(qo, row0, side="right") - 1)
+        assert kv_off == kv[b] and kv_len == kv[b + 1] - kv[b]
+        assert pos0 == kv_len - (qo[b + 1] - qo[b]) + (row0 - qo[b])
+        for r in range(row0, row0 + nrows):
+            for h in range(head0, head0 + nh):
+                rows.add((r, h))
+    assert rows == {(r, h) for r in range(350) for h in range(8)}
+    lib.attn_plan_destroy(handle)
