@@ -349,6 +349,39 @@ def run_ours(args, world, rank, local):
                 "kernel": "decode_sink_attn_kernel<64,false>", "peak_source": peak_src,
                 "frac_of_nominal_8TBps": achieved / 8000.0}
 
+    # ---- the same decode as one replay of a captured CUDA graph (device-built
+    # work list + persistent decode over it), inputs resident
+    graph = None
+    try:
+        gplan = binding.GraphPlan(batch.batch_size, batch.num_qo_heads, batch.num_kv_heads, batch.head_dim,
+                                  batch.page_size, pt, batch.num_pages, sm_scale=batch.sm_scale)
+        g_indptr = torch.from_numpy(batch.kv_indptr).to(dev)
+        g_lpl = torch.from_numpy(batch.last_page_len).to(dev)
+        g_b = torch.tensor([batch.batch_size], dtype=torch.int32, device=dev)
+        gdec = lambda: gplan.decode(q, kv, g_indptr, g_lpl, g_b, sinks, out, lse)
+        gdec()
+        torch.cuda.synchronize()
+        cg = torch.cuda.CUDAGraph()
+        cs = torch.cuda.Stream()
+        cs.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(cs):
+            with torch.cuda.graph(cg, stream=cs):
+                gdec()
+        torch.cuda.current_stream().wait_stream(cs)
+        for _ in range(args.warmup):
+            cg.replay()
+        gsteps = max(3, args.steps // 10)
+        gtimes = time_device(cg.replay, gsteps, flush, stream)
+        gmean = sum(gtimes) / len(gtimes) / 1e3
+        if gplan.device_error():
+            raise RuntimeError("graph decode recorded a device error")
+        graph = {"workload": "gptoss_decode, one CUDA-graph replay (device planner + persistent decode)",
+                 "value": bytes_step / gmean / 1e9, "unit": "GB/s", "ms_per_step": gmean * 1e3,
+                 "frac_of_hbm_peak": bytes_step / gmean / 1e9 / float(peaks["hbm_gbs"]),
+                 "launches": 2 * gsteps}
+    except binding.AttnError as e:
+        graph = {"unavailable": str(e)}
+
     # ---- e2e through the public API from pinned host buffers
     q_h = torch.from_numpy(batch.q.view(np.int16)).view(torch.bfloat16).pin_memory()
     pt_h = torch.from_numpy(batch.page_table).pin_memory()
@@ -384,7 +417,7 @@ def run_ours(args, world, rank, local):
 
     # ---- prefill leg (TFLOP/s), if the kernel is available
     prefill = None
-    launches = args.steps
+    launches = args.steps + (graph.get("launches", 0) if graph else 0)
     if not args.no_prefill:
         pbatch = syn.gptoss_prefill(seed=rank)
         pq, pkv, ppt, psk = to_dev(pbatch)
@@ -503,7 +536,7 @@ def run_ours(args, world, rank, local):
                        "parallelism": f"replicas x{world}", "plan_us": plan_us,
                        "decode_units": units},
             "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
-            "clocks": clocks, "cpu_baseline": cpu, "prefill": prefill, "prefill_ragged": ragged, "kv_cache": kvcache,
+            "clocks": clocks, "cpu_baseline": cpu, "decode_graph": graph, "prefill": prefill, "prefill_ragged": ragged, "kv_cache": kvcache,
         }
         print(json.dumps(line), flush=True)
 

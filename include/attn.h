@@ -74,6 +74,8 @@ typedef enum {
 /* Bits of the device error word (attn_plan_device_error). */
 #define ATTN_DEVICE_ERR_PAGE_ID 1      /* page id outside [0, num_pages_in_pool) */
 #define ATTN_DEVICE_ERR_TIMEOUT 2      /* a bounded wait inside a kernel ran out */
+#define ATTN_DEVICE_ERR_PLAN 4         /* attn_decode_graph: malformed request metadata or
+                                          work beyond the graph plan's capacity */
 
 /* Opaque plan; owned by the library, freed with attn_plan_destroy. */
 typedef struct attn_plan_s* attn_plan_t;
@@ -232,6 +234,51 @@ ATTN_API attn_status attn_merge_states(const void* va, const float* lsea, const 
  */
 ATTN_API attn_status attn_decode_noalloc(attn_plan_t plan, const void* q, const void* kv_cache,
                                          const float* sinks, void* out, float* lse, void* stream);
+
+/*
+ * attn_graph_plan / attn_decode_graph -- decode that can be captured in a CUDA
+ * graph and replayed for new batches.  The split-KV plan depends on the
+ * requests' lengths, so host planning would freeze it at capture; here the
+ * step's first kernel builds the work list on the device from device-resident
+ * metadata, with the same rule as attn_plan, and a fixed grid of persistent
+ * decode CTAs takes the units from a device queue ("Fast embeddings on GPUs"
+ * (Perplexity), section "Managing CUDA graphs": kernels that configure their
+ * launches from dynamic host inputs prevent full CUDA graphs; the page's fix
+ * is to change those kernels so they can be captured).
+ *
+ * attn_graph_plan sizes a plan once, for at most `max_batch` decode requests
+ * whose KV lengths sum to at most `max_kv_tokens` (0: num_pages_in_pool *
+ * page_size); bind a workspace with attn_plan_bind_workspace as usual.  The
+ * page table pointer is fixed; its contents may change between replays.
+ *
+ * attn_decode_graph reads, on the device and at run time:
+ *   batch          int32 scalar: B <= max_batch decode requests (query row b =
+ *                  request b; q / out are [max_batch][Hq][head_dim], lse
+ *                  [max_batch][Hq]; rows >= B are not touched)
+ *   kv_indptr      int32 [B + 1] page CSR into page_table, kv_indptr[0] = 0
+ *   last_page_len  int32 [B], in [1, page_size]
+ * No host synchronisation, copy or allocation happens inside the call, so it
+ * can be captured (after one uncaptured call has built the TMA descriptor for
+ * this kv_cache pointer).  A request with a malformed entry, or a batch beyond
+ * the plan's capacity, sets ATTN_DEVICE_ERR_PLAN; such requests (or, past
+ * the capacity, the whole step) produce no output.  attn_decode, attn_prefill
+ * and attn_append_kv reject graph plans.
+ */
+ATTN_API attn_status attn_graph_plan(int32_t max_batch, int32_t num_qo_heads, int32_t num_kv_heads,
+                                     int32_t head_dim, int32_t page_size, float sm_scale, int32_t num_pages_in_pool,
+                                     int64_t max_kv_tokens, const int32_t* page_table, int32_t num_sms,
+                                     attn_plan_t* plan_out, size_t* workspace_bytes_out);
+ATTN_API attn_status attn_decode_graph(attn_plan_t plan, const int32_t* kv_indptr, const int32_t* last_page_len,
+                                       const int32_t* batch, const void* q, const void* kv_cache, const float* sinks,
+                                       void* out, float* lse, void* stream);
+/*
+ * Copy the work list that the last attn_decode_graph built on the device into
+ * host memory (12 int32 per unit, as attn_plan_get_decode_units), after
+ * synchronising `stream`; *n_units receives the unit count.  For tests and
+ * inspection.
+ */
+ATTN_API attn_status attn_graph_plan_read_units(attn_plan_t plan, int32_t* units, int64_t capacity,
+                                                int64_t* n_units, void* stream);
 
 /*
  * attn_append_kv -- write the step's new K and V rows into the paged cache,

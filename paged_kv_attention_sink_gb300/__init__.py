@@ -6,7 +6,7 @@ binding is imported lazily so that ``synthetic`` (seeded inputs) can be used on
 machines without the built library; any use of the API without the library
 raises immediately -- there is no CPU fallback.
 """
-_API = ("Plan", "RaggedPlan", "attn_plan", "attn_prefill", "attn_decode", "attn_merge_states",
+_API = ("Plan", "RaggedPlan", "GraphPlan", "attn_plan", "attn_prefill", "attn_decode", "attn_merge_states",
         "attn_pack_kv_heads", "attn_unpack_kv_heads", "load_library", "library_path", "AttnError")
 
 

@@ -57,6 +57,9 @@ def _declare(lib):
         "attn_merge_states": (st, [p, p, p, p, p, p, i32, i32, i32, p]),
         "attn_append_kv": (st, [p, p, p, p, p]),
         "attn_plan_ragged": (st, [p, p, i32, i32, i32, i32, i32, f32, i32, p, p]),
+        "attn_graph_plan": (st, [i32, i32, i32, i32, i32, f32, i32, i64, p, i32, p, p]),
+        "attn_decode_graph": (st, [p, p, p, p, p, p, p, p, p, p]),
+        "attn_graph_plan_read_units": (st, [p, p, i64, p, p]),
         "attn_prefill_ragged": (st, [p, p, p, p, p, p, p, p]),
         "attn_pack_kv_heads": (st, [p, i64, i32, i32, i32, p, i64, i32, i32, p, p, p]),
         "attn_unpack_kv_heads": (st, [p, i64, i32, i32, i32, p, i64, i32, i32, p, p, p]),
@@ -290,6 +293,61 @@ class RaggedPlan(Plan):
 
     def append_kv(self, *args, **kwargs):
         raise TypeError("a ragged plan has no KV cache")
+
+
+class GraphPlan(Plan):
+    """Decode plan for CUDA-graph capture: the work list is built on the device
+    at every call from device-resident request metadata (see attn_decode_graph).
+    q / out are [max_batch, Hq, D]; lse [max_batch, Hq]."""
+
+    def __init__(self, max_batch: int, num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
+                 page_table: torch.Tensor, num_pages: int, sm_scale: Optional[float] = None,
+                 max_kv_tokens: int = 0, num_sms: int = 0, stream=None):
+        lib = load_library()
+        self._handle = None
+        if not (isinstance(page_table, torch.Tensor) and page_table.is_cuda and
+                page_table.dtype == torch.int32 and page_table.is_contiguous()):
+            raise TypeError("page_table must be a contiguous int32 CUDA tensor")
+        self.page_table = page_table
+        self.batch = self.total_rows = int(max_batch)
+        self.num_qo_heads, self.num_kv_heads = num_qo_heads, num_kv_heads
+        self.head_dim, self.page_size, self.num_pages = head_dim, page_size, num_pages
+        self.sm_scale = float(sm_scale) if sm_scale is not None else head_dim ** -0.5
+        handle = ctypes.c_void_p()
+        ws_bytes = ctypes.c_size_t()
+        _check("attn_graph_plan", lib.attn_graph_plan(
+            int(max_batch), num_qo_heads, num_kv_heads, head_dim, page_size, self.sm_scale, int(num_pages),
+            int(max_kv_tokens), _ptr(page_table), int(num_sms), ctypes.byref(handle), ctypes.byref(ws_bytes)))
+        self._handle = handle
+        self.workspace = torch.empty(max(int(ws_bytes.value), 256), dtype=torch.uint8, device=page_table.device)
+        _check("attn_plan_bind_workspace", lib.attn_plan_bind_workspace(
+            self._handle, _ptr(self.workspace), self.workspace.numel(), _stream_ptr(stream)))
+
+    def decode(self, q, kv_cache, kv_indptr, last_page_len, batch, sinks=None, out=None, lse=None, stream=None):
+        """kv_indptr [>= B+1], last_page_len [>= B], batch [1]: int32 CUDA tensors read on the device."""
+        for name, t in (("kv_indptr", kv_indptr), ("last_page_len", last_page_len), ("batch", batch)):
+            if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.int32 and t.is_contiguous()):
+                raise TypeError(f"{name} must be a contiguous int32 CUDA tensor")
+        out = torch.empty_like(q) if out is None else out
+        self._check_tensors(q, kv_cache, sinks, out, lse)
+        _check("attn_decode_graph", load_library().attn_decode_graph(
+            self._handle, _ptr(kv_indptr), _ptr(last_page_len), _ptr(batch), _ptr(q), _ptr(kv_cache), _ptr(sinks),
+            _ptr(out), _ptr(lse), _stream_ptr(stream)))
+        return out, lse
+
+    def device_units(self, stream=None) -> np.ndarray:
+        cap = self.info()["num_decode_partials"]
+        out = np.zeros((cap, 12), dtype=np.int32)
+        n = ctypes.c_int64()
+        _check("attn_graph_plan_read_units", load_library().attn_graph_plan_read_units(
+            self._handle, out.ctypes.data_as(ctypes.c_void_p), cap, ctypes.byref(n), _stream_ptr(stream)))
+        return out[:n.value]
+
+    def prefill(self, *args, **kwargs):
+        raise TypeError("a graph plan only decodes")
+
+    def append_kv(self, *args, **kwargs):
+        raise TypeError("a graph plan only decodes")
 
 
 def attn_plan(qo_indptr, kv_indptr, page_table, last_page_len, num_qo_heads, num_kv_heads,

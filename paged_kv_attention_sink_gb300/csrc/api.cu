@@ -119,6 +119,7 @@ extern "C" attn_status attn_plan_bind_workspace(attn_plan_t plan, void* workspac
 
 extern "C" attn_status attn_decode(attn_plan_t plan, const void* q, const void* kv_cache,
                                    const float* sinks, void* out, float* lse, void* stream) {
+    if (plan && plan->graph) return ATTN_ERR_INVALID_ARG;   // attn_decode_graph
     if (plan && plan->bound && plan->units.empty()) return ATTN_OK;
     attn_status st = check_launch(plan, q, kv_cache, out);
     if (st != ATTN_OK) return st;
@@ -128,6 +129,37 @@ extern "C" attn_status attn_decode(attn_plan_t plan, const void* q, const void* 
     }
     return attn::launch_decode(plan, q, plan->kv_map_decode, sinks, out, lse,
                                static_cast<cudaStream_t>(stream));
+}
+
+extern "C" attn_status attn_decode_graph(attn_plan_t plan, const int32_t* kv_indptr, const int32_t* last_page_len,
+                                         const int32_t* batch, const void* q, const void* kv_cache,
+                                         const float* sinks, void* out, float* lse, void* stream) {
+    if (!plan || !plan->graph) return ATTN_ERR_INVALID_ARG;
+    attn_status st = check_launch(plan, q, kv_cache, out);
+    if (st != ATTN_OK) return st;
+    if (!kv_indptr || !last_page_len || !batch) return ATTN_ERR_INVALID_ARG;
+    if (plan->kv_map_decode_ptr != kv_cache) {
+        if (!make_kv_map(plan->kv_map_decode, kv_cache, plan, attn::kBlockTokens)) return ATTN_ERR_CUDA;
+        plan->kv_map_decode_ptr = kv_cache;
+    }
+    return attn::launch_decode_graph(plan, kv_indptr, last_page_len, batch, q, plan->kv_map_decode, sinks, out, lse,
+                                     static_cast<cudaStream_t>(stream));
+}
+
+extern "C" attn_status attn_graph_plan_read_units(attn_plan_t plan, int32_t* units, int64_t capacity,
+                                                  int64_t* n_units, void* stream) {
+    if (!plan || !plan->graph || !n_units || capacity < 0 || (capacity > 0 && !units)) return ATTN_ERR_INVALID_ARG;
+    if (!plan->bound) return ATTN_ERR_NOT_BOUND;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+    int32_t n = 0;
+    if (cudaMemcpy(&n, plan->ws + plan->layout.n_units, sizeof n, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    *n_units = n;
+    const int64_t k = n < capacity ? n : capacity;
+    if (k > 0 && cudaMemcpy(units, plan->ws + plan->layout.units, (size_t)k * sizeof(attn::DecodeUnit),
+                            cudaMemcpyDeviceToHost) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    return ATTN_OK;
 }
 
 extern "C" attn_status attn_prefill(attn_plan_t plan, const void* q, const void* kv_cache,
@@ -190,7 +222,7 @@ extern "C" attn_status attn_merge_states(const void* va, const float* lsea, cons
 
 extern "C" attn_status attn_append_kv(attn_plan_t plan, const void* k_new, const void* v_new, void* kv_cache,
                                      void* stream) {
-    if (!plan || plan->ragged) return ATTN_ERR_INVALID_ARG;   // a ragged plan has no cache
+    if (!plan || plan->ragged || plan->graph) return ATTN_ERR_INVALID_ARG;   // no host row list
     if (!plan->bound) return ATTN_ERR_NOT_BOUND;
     if (plan->info.total_qo_rows == 0) return ATTN_OK;
     if (!k_new || !v_new || !kv_cache) return ATTN_ERR_INVALID_ARG;

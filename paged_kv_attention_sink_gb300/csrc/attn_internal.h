@@ -17,6 +17,7 @@ constexpr int kDecodeMaxChunkBlocks = 512;
 constexpr int kDecodeMaxChunkPages = kDecodeMaxChunkBlocks * kBlockTokens / 16 + 2;
 constexpr int kPrefillRows = 128;         // query rows per prefill tile (TMEM lanes)
 constexpr int kPrefillKeys = 128;         // keys per prefill KV tile
+constexpr int kGraphMaxBatch = 4096;      // attn_graph_plan: requests the device planner can order
 
 // One decode CTA: a chunk [tok_begin, tok_end) of one request's KV sequence for
 // one KV head and up to 16 of its query heads.
@@ -55,8 +56,8 @@ struct PrefillItem {
 static_assert(sizeof(PrefillItem) == 48, "prefill item is 12 int32");
 
 struct WorkspaceLayout {
-    size_t units = 0, items = 0, item_off = 0, append = 0, counters = 0, err = 0, part_lse = 0, part_o = 0,
-           total = 0;
+    size_t units = 0, items = 0, item_off = 0, append = 0, counters = 0, err = 0, n_units = 0, part_lse = 0,
+           part_o = 0, total = 0;
 };
 
 // CTAs of the decode kernel resident per SM for a head dim (matches its
@@ -72,6 +73,8 @@ struct attn_plan_s {
     int32_t num_sms = 0;
     const int32_t* page_table = nullptr;  // device, borrowed
     bool ragged = false;                  // contiguous K / V (attn_plan_ragged), no page table
+    bool graph = false;                   // attn_graph_plan: decode work list built on the device
+                                          // (batch = max batch; n_partials / n_groups = capacities)
     int64_t kv_tokens = 0;                // ragged: rows of K and V (kv_indptr[batch])
 
     std::vector<attn::DecodeUnit> units;

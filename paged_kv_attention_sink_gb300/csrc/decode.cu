@@ -44,7 +44,7 @@ struct DecodeCfg {
     static constexpr int kPipeBytes = kWarps * kStages * kStageBytes;
     static constexpr int kPageBytes = (kDecodeMaxChunkPages * 4 + 15) / 16 * 16;
     static constexpr int kBarBytes = kWarps * kStages * 8;
-    static constexpr int kStateBytes = kWarps * 48 * 4 + 16;  // per-warp m, l, le + flag
+    static constexpr int kStateBytes = kWarps * 48 * 4 + 16;  // per-warp m, l, le + flags
     static constexpr int kSmem = 1024 + kPipeBytes + kPageBytes + kBarBytes + kStateBytes;
     static constexpr int kRowStride = D + 8;                  // floats, combine buffers
     static_assert(kBlockTokens * kRowStride * 4 <= kStages * kStageBytes, "combine fits");
@@ -59,7 +59,9 @@ struct DecodeArgs {
     const float* sinks;
     float* part_o;
     float* part_lse;
-    int32_t* counters;
+    int32_t* counters;  // split-merge tickets, one per split group
+    int32_t* queue;     // persistent launches: [0] next unit to hand out, [1] CTAs finished
+    const int32_t* n_units_dev;   // persistent launches: unit count, written on the device
     int32_t* err;
     int32_t Hq, Hkv, P, num_pages;
     float scale_log2;   // sm_scale * log2(e)
@@ -76,7 +78,12 @@ __device__ __forceinline__ void store_bf16x4(__nv_bfloat16* dst, float a, float 
     *reinterpret_cast<uint2*>(dst) = v;
 }
 
-template <int D, bool kTwoRows>
+// kPersistent = false: CTA c runs unit c (grid = unit count, host-planned).
+// kPersistent = true: a fixed grid takes units from a device queue until the
+// device-written unit count is reached (the CUDA-graph path, whose work list
+// is built on the device, so neither the grid nor the count is known on the
+// host).
+template <int D, bool kTwoRows, bool kPersistent>
 __global__ void __launch_bounds__(kDecodeWarps * 32)
 decode_sink_attn_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
     using C = DecodeCfg<D>;
@@ -91,24 +98,41 @@ decode_sink_attn_kernel(const __grid_constant__ CUtensorMap kv_map, const Decode
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gq = lane >> 2, tq = lane & 3;
-    const DecodeUnit u = a.units[blockIdx.x];
     const int P = a.P;
-    const int first_page = u.tok_begin / P;
-    const int n_pages = (u.tok_end - 1) / P - first_page + 1;
+    volatile int* unit_s = flag_s + 1;   // unit handed to this CTA
+    volatile int* abort_s = flag_s + 2;
 
-    for (int i = tid; i < n_pages; i += blockDim.x)
-        pages_s[i] = a.page_table[u.page_base + first_page + i];
     if (lane == 0)
         for (int s = 0; s < C::kStages; ++s) ptx::mbar_init(ptx::smem_u32(&bars[warp * C::kStages + s]), 1);
-    if (tid == 0) ptx::prefetch_tmap(&kv_map);
+    if (tid == 0) {
+        ptx::prefetch_tmap(&kv_map);
+        *abort_s = 0;
+    }
     ptx::fence_mbar_init();
+
+    const uint32_t stage0 = ptx::smem_u32(pipe) + warp * C::kStages * C::kStageBytes;
+    const uint32_t bar0 = ptx::smem_u32(&bars[warp * C::kStages]);
+    const uint64_t policy = ptx::policy_evict_first();
+    int gbase = 0;   // stage uses of this warp's ring so far (across units)
+
+    const int n_units = kPersistent ? *a.n_units_dev : 0;
+    while (true) {
+    int unit = blockIdx.x;
+    if constexpr (kPersistent) {
+        if (tid == 0) *unit_s = atomicAdd(&a.queue[0], 1);
+        __syncthreads();
+        unit = *unit_s;
+        if (unit >= n_units || *abort_s) break;
+    }
+    const DecodeUnit u = a.units[unit];
+    const int first_page = u.tok_begin / P;
+    const int n_pages = (u.tok_end - 1) / P - first_page + 1;
+    for (int i = tid; i < n_pages; i += blockDim.x)
+        pages_s[i] = a.page_table[u.page_base + first_page + i];
     __syncthreads();
 
     const int nblk = (u.tok_end - u.tok_begin + kBlockTokens - 1) / kBlockTokens;
     const int n_it = nblk > warp ? (nblk - warp + C::kWarps - 1) / C::kWarps : 0;
-    const uint32_t stage0 = ptx::smem_u32(pipe) + warp * C::kStages * C::kStageBytes;
-    const uint32_t bar0 = ptx::smem_u32(&bars[warp * C::kStages]);
-    const uint64_t policy = ptx::policy_evict_first();
 
     // Lane 0: start the loads of block kb into stage s.
     auto issue = [&](int kb, int s) {
@@ -134,7 +158,7 @@ decode_sink_attn_kernel(const __grid_constant__ CUtensorMap kv_map, const Decode
     };
 
     if (lane == 0)
-        for (int it = 0; it < C::kStages && it < n_it; ++it) issue(warp + it * C::kWarps, it);
+        for (int it = 0; it < C::kStages && it < n_it; ++it) issue(warp + it * C::kWarps, (gbase + it) % C::kStages);
 
     // Q fragments (A operand, rows = query heads of the slice).
     uint32_t qa[D / 16][4];
@@ -174,8 +198,8 @@ decode_sink_attn_kernel(const __grid_constant__ CUtensorMap kv_map, const Decode
     int it = 0;
     bool timed_out = false;
     for (; it < n_it; ++it) {
-        const int s = it % C::kStages;
-        if (!ptx::mbar_wait(bar0 + s * 8, (it / C::kStages) & 1)) { timed_out = true; break; }
+        const int s = (gbase + it) % C::kStages;
+        if (!ptx::mbar_wait(bar0 + s * 8, ((gbase + it) / C::kStages) & 1)) { timed_out = true; break; }
         const int kb = warp + it * C::kWarps;
         const int valid = min(kBlockTokens, u.tok_end - (u.tok_begin + kb * kBlockTokens));
         const uint32_t kt = stage0 + s * C::kStageBytes;
@@ -288,10 +312,14 @@ decode_sink_attn_kernel(const __grid_constant__ CUtensorMap kv_map, const Decode
         }
     }
     if (timed_out) {
-        if (lane == 0) atomicOr(a.err, ATTN_DEVICE_ERR_TIMEOUT);
+        if (lane == 0) {
+            atomicOr(a.err, ATTN_DEVICE_ERR_TIMEOUT);
+            *abort_s = 1;
+        }
         for (int j = it; j < n_it && j < it + C::kStages; ++j)   // drain loads still in flight
-            ptx::mbar_wait(bar0 + (j % C::kStages) * 8, (j / C::kStages) & 1);
+            ptx::mbar_wait(bar0 + ((gbase + j) % C::kStages) * 8, ((gbase + j) / C::kStages) & 1);
     }
+    gbase += n_it;
 
     // Row sums over the quad, then this warp's state into its own stage area.
     l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
@@ -352,8 +380,7 @@ decode_sink_attn_kernel(const __grid_constant__ CUtensorMap kv_map, const Decode
             if (d == 0) a.part_lse[slot] = lse2;
         }
     }
-    if (u.n_chunks == 1) return;
-
+    if (u.n_chunks > 1) {
     // Split sequence: the last chunk to finish merges all chunks (no waiting).
     __threadfence();
     __syncthreads();
@@ -362,7 +389,7 @@ decode_sink_attn_kernel(const __grid_constant__ CUtensorMap kv_map, const Decode
         *flag_s = (prev == u.n_chunks - 1);
     }
     __syncthreads();
-    if (!*flag_s) return;
+    if (*flag_s) {
     __threadfence();
     for (int idx = tid; idx < items; idx += blockDim.x) {
         const int r = idx / (D / 4), d = (idx % (D / 4)) * 4;
@@ -386,20 +413,295 @@ decode_sink_attn_kernel(const __grid_constant__ CUtensorMap kv_map, const Decode
             a.lse[(size_t)u.q_row * a.Hq + u.head0 + r] = (W > 0.f ? Lm + log2f(W) : -INFINITY) * kLn2;
     }
     if (tid == 0) a.counters[u.group] = 0;   // ready for the next launch
+    }
+    }
+    if constexpr (!kPersistent) break;
+    __syncthreads();   // shared memory is reused by the next unit
+    }
+
+    // The last CTA to finish resets the queue for the next launch.
+    if (kPersistent && tid == 0) {
+        __threadfence();
+        if (atomicAdd(&a.queue[1], 1) == (int)gridDim.x - 1) {
+            atomicExch(&a.queue[0], 0);
+            atomicExch(&a.queue[1], 0);
+        }
+    }
 }
 
-template <int D, bool kTwoRows>
-cudaError_t launch(const CUtensorMap& map, const DecodeArgs& args, int n_units, cudaStream_t stream) {
+// ------------------------------------------------------------ device planner
+// The CUDA-graph decode path plans on the device: the same split rule as the
+// host planner, from request metadata that lives in device memory, so that a
+// captured graph replays with new lengths and batch sizes (decode requests
+// only: request b is query row b).  One CTA; each thread owns a contiguous
+// range of requests.
+constexpr int kPlanThreads = 1024;
+
+struct GraphPlanArgs {
+    const int32_t* kv_indptr;       // [batch + 1] page CSR
+    const int32_t* last_page_len;   // [batch]
+    const int32_t* batch;           // device scalar
+    int32_t max_batch, Hq, Hkv, P, n_slices;
+    int64_t target_units;
+    int32_t cap_units, cap_groups;
+    DecodeUnit* units;
+    int32_t* n_units;
+    int32_t* queue;                 // [2], then the split-merge counters
+    int32_t* err;
+};
+
+// Exclusive block-wide scan of three counters (kPlanThreads threads).
+__device__ void block_scan3(int (&v)[3], int (&total)[3], int* sh /* [3][32] */) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int inc[3] = {v[0], v[1], v[2]};
+#pragma unroll
+    for (int k = 0; k < 3; ++k)
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, inc[k], o);
+            if (lane >= o) inc[k] += n;
+        }
+    if (lane == 31)
+        for (int k = 0; k < 3; ++k) sh[k * 32 + warp] = inc[k];
+    __syncthreads();
+    if (warp == 0)
+        for (int k = 0; k < 3; ++k) {
+            int w = sh[k * 32 + lane];
+            for (int o = 1; o < 32; o <<= 1) {
+                const int n = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += n;
+            }
+            sh[k * 32 + lane] = w;   // inclusive over warps
+        }
+    __syncthreads();
+    for (int k = 0; k < 3; ++k) {
+        total[k] = sh[k * 32 + 31];
+        v[k] = inc[k] - v[k] + (warp > 0 ? sh[k * 32 + warp - 1] : 0);
+    }
+    __syncthreads();
+}
+
+// Dynamic shared memory of the planner: 7 int32 per request slot (page
+// base, kv_len, sorted order, chunk count, and the exclusive offsets of units,
+// partial slots and groups).
+inline size_t plan_smem_bytes(int max_batch) { return (size_t)max_batch * 7 * sizeof(int); }
+
+// Token range [c * nblk / nc, (c + 1) * nblk / nc) blocks, in 32-bit
+// arithmetic when the product fits (the common case).
+__device__ __forceinline__ int64_t chunk_block(int c, int64_t nblk, int nc) {
+    const uint64_t prod = (uint64_t)c * (uint64_t)nblk;
+    return prod < 0xFFFFFFFFull ? (int64_t)((uint32_t)prod / (uint32_t)nc) : (int64_t)(prod / (uint64_t)nc);
+}
+
+__global__ void __launch_bounds__(kPlanThreads) decode_graph_plan_kernel(const GraphPlanArgs p) {
+    extern __shared__ int plan_smem[];
+    constexpr int kLenBuckets = kDecodeMaxChunkBlocks + 1;   // unit length 0 (malformed) .. 512 blocks
+    __shared__ int s_hist[kLenBuckets];
+    __shared__ long long s_blocks[32];
+    __shared__ int s_scan[3 * 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int* s_base = plan_smem;                 // [max_batch] kv_indptr[b]
+    int* s_kv = s_base + p.max_batch;        // [max_batch] kv_len, -1 malformed
+    int* s_order = s_kv + p.max_batch;       // [max_batch] request at sorted position i
+    int* s_nc = s_order + p.max_batch;       // [max_batch] chunks (sorted order)
+    int* s_uoff = s_nc + p.max_batch;        // [max_batch] exclusive offsets (sorted order)
+    int* s_poff = s_uoff + p.max_batch;
+    int* s_goff = s_poff + p.max_batch;
+
+    int B = *p.batch;
+    if (B < 0 || B > p.max_batch) {
+        if (tid == 0) atomicOr(p.err, ATTN_DEVICE_ERR_PLAN);
+        B = B < 0 ? 0 : p.max_batch;
+    }
+    for (int k = tid; k < kLenBuckets; k += kPlanThreads) s_hist[k] = 0;
+
+    // Pass 1: kv lengths, and all 16-token blocks -> chunk size (two waves of CTAs).
+    long long blocks = 0;
+    for (int b = tid; b < B; b += kPlanThreads) {
+        const int32_t base = p.kv_indptr[b];
+        const int64_t np = (int64_t)p.kv_indptr[b + 1] - base;
+        const int32_t lpl = p.last_page_len[b];
+        int64_t kv = -1;
+        if (np >= 1 && lpl >= 1 && lpl <= p.P) kv = (np - 1) * p.P + lpl;
+        if (kv < 0 || kv > INT32_MAX) {
+            atomicOr(p.err, ATTN_DEVICE_ERR_PLAN);
+            kv = -1;
+        }
+        s_base[b] = base;
+        s_kv[b] = (int)kv;
+        if (kv > 0) blocks += (kv + kBlockTokens - 1) / kBlockTokens;
+    }
+    for (int o = 16; o > 0; o >>= 1) blocks += __shfl_xor_sync(0xffffffffu, blocks, o);
+    if (lane == 0) s_blocks[warp] = blocks;
+    __syncthreads();
+    long long total_blocks = 0;
+    for (int w = 0; w < kPlanThreads / 32; ++w) total_blocks += s_blocks[w];
+    total_blocks *= (long long)p.Hkv * p.n_slices;
+    int64_t chunk = (int64_t)((total_blocks + p.target_units - 1) / p.target_units);
+    chunk = min((int64_t)kDecodeMaxChunkBlocks, max((int64_t)kDecodeMinChunkBlocks, chunk));
+    auto n_chunks_of = [&](int64_t kv) -> int {
+        if (kv < 0) return 0;
+        const int64_t nblk = (kv + kBlockTokens - 1) / kBlockTokens;
+        int64_t n = max((int64_t)1, (nblk + chunk / 2) / chunk);
+        n = max(n, (int64_t)((nblk + kDecodeMaxChunkBlocks - 1) / kDecodeMaxChunkBlocks));
+        return (int)n;
+    };
+    auto unit_len = [&](int64_t kv, int nc) -> int {   // blocks in the request's longest chunk
+        return nc > 0 ? (int)(((kv + kBlockTokens - 1) / kBlockTokens + nc - 1) / nc) : 0;
+    };
+
+    // Pass 2: order the requests by unit length, longest first (counting sort
+    // over the 513 possible lengths), as the host planner orders its units.
+    for (int b = tid; b < B; b += kPlanThreads) {
+        const int64_t kv = s_kv[b];
+        atomicAdd(&s_hist[kDecodeMaxChunkBlocks - unit_len(kv, n_chunks_of(kv))], 1);
+    }
+    __syncthreads();
+    if (warp == 0) {   // exclusive scan of the histogram, 17 buckets per lane
+        constexpr int kPer = (kLenBuckets + 31) / 32;
+        int local[kPer], sum = 0;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int idx = lane * kPer + k;
+            local[k] = idx < kLenBuckets ? s_hist[idx] : 0;
+            sum += local[k];
+        }
+        int inc = sum;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += n;
+        }
+        int run = inc - sum;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int idx = lane * kPer + k;
+            if (idx < kLenBuckets) s_hist[idx] = run;
+            run += local[k];
+        }
+    }
+    __syncthreads();
+    for (int b = tid; b < B; b += kPlanThreads) {
+        const int64_t kv = s_kv[b];
+        s_order[atomicAdd(&s_hist[kDecodeMaxChunkBlocks - unit_len(kv, n_chunks_of(kv))], 1)] = b;
+    }
+    __syncthreads();
+
+    // Pass 3: units, partial slots and groups in sorted order, scanned (each
+    // thread a contiguous range of sorted positions).
+    const int per_req = p.Hkv * p.n_slices;
+    const int per = (B + kPlanThreads - 1) / kPlanThreads;
+    const int i0 = min(B, tid * per), i1 = min(B, i0 + per);
+    int v[3] = {0, 0, 0}, tot[3];
+    for (int i = i0; i < i1; ++i) {
+        const int nc = n_chunks_of(s_kv[s_order[i]]);
+        s_nc[i] = nc;
+        v[0] += nc * per_req;
+        if (nc > 1) {
+            v[1] += nc * per_req;
+            v[2] += per_req;
+        }
+    }
+    block_scan3(v, tot, s_scan);
+    if (tot[0] > p.cap_units || tot[1] > p.cap_units || tot[2] > p.cap_groups) {
+        if (tid == 0) {
+            atomicOr(p.err, ATTN_DEVICE_ERR_PLAN);
+            *p.n_units = 0;
+            p.queue[0] = p.queue[1] = 0;
+        }
+        return;
+    }
+    for (int i = i0; i < i1; ++i) {
+        s_uoff[i] = v[0];
+        s_poff[i] = v[1];
+        s_goff[i] = v[2];
+        const int nc = s_nc[i];
+        v[0] += nc * per_req;
+        if (nc > 1) {
+            v[1] += nc * per_req;
+            v[2] += per_req;
+        }
+    }
+    __syncthreads();
+
+    // Pass 4: one warp per sorted request, its lanes over the request's units
+    // (head slice major, chunk minor; chunk 0 of a group carries the sink);
+    // each unit is written as three 16-byte stores.
+    const int G = p.Hq / p.Hkv;
+    for (int i = warp; i < B; i += kPlanThreads / 32) {
+        const int nc = s_nc[i];
+        if (nc == 0) continue;
+        const int b = s_order[i];
+        const int64_t kv = s_kv[b];
+        const int64_t nblk = (kv + kBlockTokens - 1) / kBlockTokens;
+        const int base = s_base[b], uoff = s_uoff[i], goff = s_goff[i], poff = s_poff[i];
+        for (int k = lane; k < nc * per_req; k += 32) {
+            const int gs = k / nc, c = k - gs * nc;
+            const int g = gs / p.n_slices, sl = gs - g * p.n_slices;
+            const int tok0 = (int)(chunk_block(c, nblk, nc) * kBlockTokens);
+            const int tok1 = (int)min(kv, chunk_block(c + 1, nblk, nc) * kBlockTokens);
+            int4* dst = reinterpret_cast<int4*>(p.units + uoff + k);
+            dst[0] = make_int4(b, base, g, g * G + sl * kMaxSliceHeads);
+            dst[1] = make_int4(min(kMaxSliceHeads, G - sl * kMaxSliceHeads), tok0, tok1, c);
+            dst[2] = make_int4(nc, nc > 1 ? goff + gs : -1, nc > 1 ? poff + gs * nc : 0, 0);
+        }
+    }
+    for (int k = tid; k < tot[2]; k += kPlanThreads) p.queue[2 + k] = 0;
+    if (tid == 0) {
+        *p.n_units = tot[0];
+        p.queue[0] = p.queue[1] = 0;
+    }
+}
+
+template <int D, bool kTwoRows, bool kPersistent>
+cudaError_t launch(const CUtensorMap& map, const DecodeArgs& args, int grid, cudaStream_t stream) {
     using C = DecodeCfg<D>;
-    auto kernel = decode_sink_attn_kernel<D, kTwoRows>;
+    auto kernel = decode_sink_attn_kernel<D, kTwoRows, kPersistent>;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    kernel<<<n_units, C::kWarps * 32, C::kSmem, stream>>>(map, args);
+    kernel<<<grid, C::kWarps * 32, C::kSmem, stream>>>(map, args);
     return cudaGetLastError();
+}
+
+template <bool kPersistent>
+attn_status dispatch(const attn_plan_s* plan, const CUtensorMap& map, const DecodeArgs& a, int grid,
+                     cudaStream_t stream) {
+    const bool two_rows = plan->Hq / plan->Hkv > 8;
+    cudaError_t e;
+    if (plan->D == 64)
+        e = two_rows ? launch<64, true, kPersistent>(map, a, grid, stream)
+                     : launch<64, false, kPersistent>(map, a, grid, stream);
+    else
+        e = two_rows ? launch<128, true, kPersistent>(map, a, grid, stream)
+                     : launch<128, false, kPersistent>(map, a, grid, stream);
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+// Kernel arguments with the plan's device regions taken from `base` (the bound
+// workspace, or the caller's scratch laid out the same way).
+DecodeArgs make_args(const attn_plan_s* plan, unsigned char* base, const void* q, const float* sinks, void* out,
+                     float* lse) {
+    DecodeArgs a;
+    a.units = reinterpret_cast<const DecodeUnit*>(base + plan->layout.units);
+    a.page_table = plan->page_table;
+    a.q = static_cast<const __nv_bfloat16*>(q);
+    a.out = static_cast<__nv_bfloat16*>(out);
+    a.lse = lse;
+    a.sinks = sinks;
+    a.part_o = reinterpret_cast<float*>(base + plan->layout.part_o);
+    a.part_lse = reinterpret_cast<float*>(base + plan->layout.part_lse);
+    a.counters = reinterpret_cast<int32_t*>(base + plan->layout.counters);
+    a.queue = nullptr;
+    a.n_units_dev = nullptr;
+    a.err = reinterpret_cast<int32_t*>(base + plan->layout.err);
+    a.Hq = plan->Hq;
+    a.Hkv = plan->Hkv;
+    a.P = plan->P;
+    a.num_pages = plan->num_pages;
+    a.scale_log2 = plan->sm_scale * kLog2e;
+    return a;
 }
 
 }  // namespace
@@ -413,66 +715,53 @@ int decode_ctas_per_sm(int head_dim) {
 attn_status launch_decode(attn_plan_s* plan, const void* q, const void* kv_map, const float* sinks,
                           void* out, float* lse, cudaStream_t stream) {
     if (plan->units.empty()) return ATTN_OK;
-    DecodeArgs a;
-    a.units = reinterpret_cast<const DecodeUnit*>(plan->ws + plan->layout.units);
-    a.page_table = plan->page_table;
-    a.q = static_cast<const __nv_bfloat16*>(q);
-    a.out = static_cast<__nv_bfloat16*>(out);
-    a.lse = lse;
-    a.sinks = sinks;
-    a.part_o = reinterpret_cast<float*>(plan->ws + plan->layout.part_o);
-    a.part_lse = reinterpret_cast<float*>(plan->ws + plan->layout.part_lse);
-    a.counters = reinterpret_cast<int32_t*>(plan->ws + plan->layout.counters);
-    a.err = reinterpret_cast<int32_t*>(plan->ws + plan->layout.err);
-    a.Hq = plan->Hq;
-    a.Hkv = plan->Hkv;
-    a.P = plan->P;
-    a.num_pages = plan->num_pages;
-    a.scale_log2 = plan->sm_scale * kLog2e;
-    const CUtensorMap& map = *static_cast<const CUtensorMap*>(kv_map);
-    const bool two_rows = plan->Hq / plan->Hkv > 8;
-    const int n = (int)plan->units.size();
-    cudaError_t e;
-    if (plan->D == 64)
-        e = two_rows ? launch<64, true>(map, a, n, stream) : launch<64, false>(map, a, n, stream);
-    else
-        e = two_rows ? launch<128, true>(map, a, n, stream) : launch<128, false>(map, a, n, stream);
-    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+    const DecodeArgs a = make_args(plan, plan->ws, q, sinks, out, lse);
+    return dispatch<false>(plan, *static_cast<const CUtensorMap*>(kv_map), a, (int)plan->units.size(), stream);
 }
-
-}  // namespace attn
-
-namespace attn {
 
 attn_status launch_decode_scratch(attn_plan_s* plan, unsigned char* scratch, const void* q,
                                   const void* kv_map, const float* sinks, void* out, float* lse,
                                   cudaStream_t stream) {
     if (plan->units.empty()) return ATTN_OK;
-    DecodeArgs a;
-    a.units = reinterpret_cast<const DecodeUnit*>(scratch + plan->layout.units);
-    a.page_table = plan->page_table;
-    a.q = static_cast<const __nv_bfloat16*>(q);
-    a.out = static_cast<__nv_bfloat16*>(out);
-    a.lse = lse;
-    a.sinks = sinks;
-    a.part_o = reinterpret_cast<float*>(scratch + plan->layout.part_o);
-    a.part_lse = reinterpret_cast<float*>(scratch + plan->layout.part_lse);
-    a.counters = reinterpret_cast<int32_t*>(scratch + plan->layout.counters);
-    a.err = reinterpret_cast<int32_t*>(scratch + plan->layout.err);
-    a.Hq = plan->Hq;
-    a.Hkv = plan->Hkv;
-    a.P = plan->P;
-    a.num_pages = plan->num_pages;
-    a.scale_log2 = plan->sm_scale * kLog2e;
-    const CUtensorMap& map = *static_cast<const CUtensorMap*>(kv_map);
-    const bool two_rows = plan->Hq / plan->Hkv > 8;
-    const int n = (int)plan->units.size();
-    cudaError_t e;
-    if (plan->D == 64)
-        e = two_rows ? launch<64, true>(map, a, n, stream) : launch<64, false>(map, a, n, stream);
-    else
-        e = two_rows ? launch<128, true>(map, a, n, stream) : launch<128, false>(map, a, n, stream);
-    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+    const DecodeArgs a = make_args(plan, scratch, q, sinks, out, lse);
+    return dispatch<false>(plan, *static_cast<const CUtensorMap*>(kv_map), a, (int)plan->units.size(), stream);
+}
+
+attn_status launch_decode_graph(attn_plan_s* plan, const int32_t* kv_indptr, const int32_t* last_page_len,
+                                const int32_t* batch, const void* q, const void* kv_map, const float* sinks,
+                                void* out, float* lse, cudaStream_t stream) {
+    GraphPlanArgs gp;
+    gp.kv_indptr = kv_indptr;
+    gp.last_page_len = last_page_len;
+    gp.batch = batch;
+    gp.max_batch = plan->batch;
+    gp.Hq = plan->Hq;
+    gp.Hkv = plan->Hkv;
+    gp.P = plan->P;
+    gp.n_slices = (plan->Hq / plan->Hkv + kMaxSliceHeads - 1) / kMaxSliceHeads;
+    gp.target_units = 2LL * plan->num_sms * decode_ctas_per_sm(plan->D);
+    gp.cap_units = plan->n_partials;   // graph plans size units and partial slots alike
+    gp.cap_groups = plan->n_groups;
+    gp.units = reinterpret_cast<DecodeUnit*>(plan->ws + plan->layout.units);
+    gp.n_units = reinterpret_cast<int32_t*>(plan->ws + plan->layout.n_units);
+    gp.queue = reinterpret_cast<int32_t*>(plan->ws + plan->layout.counters);
+    gp.err = reinterpret_cast<int32_t*>(plan->ws + plan->layout.err);
+    const size_t smem = plan_smem_bytes(plan->batch);
+    static size_t configured = 0;
+    if (smem > 48 * 1024 && smem > configured) {
+        if (cudaFuncSetAttribute(decode_graph_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return ATTN_ERR_CUDA;
+        configured = smem;
+    }
+    decode_graph_plan_kernel<<<1, kPlanThreads, smem, stream>>>(gp);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    DecodeArgs a = make_args(plan, plan->ws, q, sinks, out, lse);
+    a.queue = gp.queue;
+    a.counters = gp.queue + 2;
+    a.n_units_dev = gp.n_units;
+    const int grid = plan->num_sms * decode_ctas_per_sm(plan->D);
+    return dispatch<true>(plan, *static_cast<const CUtensorMap*>(kv_map), a, grid, stream);
 }
 
 }  // namespace attn

@@ -16,6 +16,10 @@ attn_status launch_prefill(attn_plan_s* plan, const void* q_map, const void* kv_
 attn_status launch_merge_states(const void* va, const float* lsea, const void* vb,
                                 const float* lseb, void* vout, float* lseout, int64_t rows,
                                 int head_dim, cudaStream_t stream);
+// CUDA-graph decode: device planner + persistent decode over its work list.
+attn_status launch_decode_graph(attn_plan_s* plan, const int32_t* kv_indptr, const int32_t* last_page_len,
+                                const int32_t* batch, const void* q, const void* kv_map, const float* sinks,
+                                void* out, float* lse, cudaStream_t stream);
 // New K/V rows of the plan's query rows into their HND page slots.
 attn_status launch_append_kv(attn_plan_s* plan, const void* k_new, const void* v_new, void* kv_cache,
                              cudaStream_t stream);

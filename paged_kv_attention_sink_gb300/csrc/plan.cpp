@@ -234,6 +234,7 @@ attn_status make_plan(bool ragged, const int32_t* qo_indptr, const int32_t* kv_i
     L.item_off = off; off = align_up(off + plan->item_off.size() * sizeof(int32_t), 256);
     L.counters = off; off = align_up(off + (size_t)plan->n_groups * sizeof(int32_t), 256);
     L.err = off;      off = align_up(off + sizeof(int32_t), 256);
+    L.n_units = off;  off = align_up(off + sizeof(int32_t), 256);
     L.part_lse = off; off = align_up(off + (size_t)plan->n_partials * kMaxSliceHeads * sizeof(float), 256);
     L.part_o = off;   off = align_up(off + (size_t)plan->n_partials * kMaxSliceHeads * head_dim * sizeof(float), 256);
     L.total = off;
@@ -312,4 +313,82 @@ extern "C" const char* attn_status_string(attn_status status) {
         case ATTN_ERR_DEVICE: return "device-side error recorded";
     }
     return "unknown status";
+}
+
+extern "C" attn_status attn_graph_plan(int32_t max_batch, int32_t num_qo_heads, int32_t num_kv_heads,
+                                       int32_t head_dim, int32_t page_size, float sm_scale,
+                                       int32_t num_pages_in_pool, int64_t max_kv_tokens,
+                                       const int32_t* page_table, int32_t num_sms, attn_plan_t* plan_out,
+                                       size_t* workspace_bytes_out) {
+    using namespace attn;
+    if (!plan_out || !workspace_bytes_out || max_batch <= 0 || !page_table || num_pages_in_pool <= 0)
+        return ATTN_ERR_INVALID_ARG;
+    if (num_qo_heads <= 0 || num_kv_heads <= 0 || num_qo_heads % num_kv_heads != 0) return ATTN_ERR_INVALID_ARG;
+    if (!std::isfinite(sm_scale) || !(sm_scale > 0.f) || page_size <= 0 || num_sms < 0 || max_kv_tokens < 0)
+        return ATTN_ERR_INVALID_ARG;
+    if (!supported_head_dim(head_dim) || !supported_page_size(page_size)) return ATTN_ERR_UNSUPPORTED;
+    if ((int64_t)max_batch * num_qo_heads > (int64_t)INT32_MAX) return ATTN_ERR_UNSUPPORTED;
+    if (max_batch > kGraphMaxBatch) return ATTN_ERR_UNSUPPORTED;   // the device planner's shared memory
+    if (num_sms == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return ATTN_ERR_CUDA;
+        }
+    }
+    // Capacity of the device-built work list.  With the host planner's rule
+    // (chunk >= total blocks / target, at most 512 blocks, each request at
+    // least one chunk per head slice) the units never exceed
+    //   target + (batch + kv_blocks / 512 + 1) * Hkv * slices,
+    // kv_blocks bounded by the tokens the batch may hold in total (default:
+    // the whole pool) plus one partial block per request.
+    const int64_t kv_tokens = max_kv_tokens > 0 ? max_kv_tokens : (int64_t)num_pages_in_pool * page_size;
+    const int64_t slices = (num_qo_heads / num_kv_heads + kMaxSliceHeads - 1) / kMaxSliceHeads;
+    const int64_t target = 2LL * num_sms * decode_ctas_per_sm(head_dim);
+    const int64_t kv_blocks = kv_tokens / kBlockTokens + max_batch;
+    const int64_t cap_units = target + (max_batch + kv_blocks / kDecodeMaxChunkBlocks + 1) * num_kv_heads * slices;
+    const int64_t cap_groups = (int64_t)max_batch * num_kv_heads * slices;
+    if (cap_units > (int64_t)INT32_MAX / kMaxSliceHeads / 256) return ATTN_ERR_UNSUPPORTED;
+
+    attn_plan_s* plan = new (std::nothrow) attn_plan_s();
+    if (!plan) return ATTN_ERR_INVALID_ARG;
+    plan->graph = true;
+    plan->batch = max_batch;
+    plan->Hq = num_qo_heads;
+    plan->Hkv = num_kv_heads;
+    plan->D = head_dim;
+    plan->P = page_size;
+    plan->causal = 1;
+    plan->sm_scale = sm_scale;
+    plan->num_pages = num_pages_in_pool;
+    plan->num_sms = num_sms;
+    plan->page_table = page_table;
+    plan->n_partials = (int32_t)cap_units;
+    plan->n_groups = (int32_t)cap_groups;
+
+    WorkspaceLayout& L = plan->layout;
+    size_t off = 0;
+    L.units = off;    off = align_up(off + (size_t)cap_units * sizeof(DecodeUnit), 256);
+    L.items = off;
+    L.item_off = off;
+    L.append = off;
+    L.counters = off; off = align_up(off + (size_t)(2 + cap_groups) * sizeof(int32_t), 256);
+    L.err = off;      off = align_up(off + sizeof(int32_t), 256);
+    L.n_units = off;  off = align_up(off + sizeof(int32_t), 256);
+    L.part_lse = off; off = align_up(off + (size_t)cap_units * kMaxSliceHeads * sizeof(float), 256);
+    L.part_o = off;   off = align_up(off + (size_t)cap_units * kMaxSliceHeads * head_dim * sizeof(float), 256);
+    L.total = off;
+
+    attn_plan_info& I = plan->info;
+    I.batch = max_batch;
+    I.total_qo_rows = max_batch;
+    I.num_decode_requests = max_batch;
+    I.num_decode_groups_split = (int32_t)cap_groups;
+    I.num_decode_partials = (int32_t)cap_units;
+    I.num_sms = num_sms;
+    I.workspace_bytes = L.total;
+    *plan_out = plan;
+    *workspace_bytes_out = L.total;
+    return ATTN_OK;
 }

@@ -1,0 +1,164 @@
+"""GPU tests of the CUDA-graph decode path (attn_graph_plan + attn_decode_graph):
+the work list is built on the device from device-resident request metadata,
+so one captured graph replays for new batches ("Fast embeddings on GPUs",
+section "Managing CUDA graphs": kernels configured from dynamic host inputs
+prevent full CUDA graphs).  Parity is against the fp64 oracle; the device
+planner is also checked unit for unit against the host planner.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import check_close, make_plan, sample_pairs, syn, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+class Buffers:
+    """Fixed device buffers a captured graph reads; each batch is copied in."""
+
+    def __init__(self, max_batch, Hq, Hkv, D, P, max_pages, max_slots):
+        dev = "cuda"
+        self.q = torch.zeros((max_batch, Hq, D), dtype=torch.bfloat16, device=dev)
+        self.out = torch.zeros_like(self.q)
+        self.lse = torch.zeros((max_batch, Hq), dtype=torch.float32, device=dev)
+        self.kv = torch.zeros((max_pages, 2, Hkv, P, D), dtype=torch.bfloat16, device=dev)
+        self.pt = torch.zeros(max_slots, dtype=torch.int32, device=dev)
+        self.kv_indptr = torch.zeros(max_batch + 1, dtype=torch.int32, device=dev)
+        self.lpl = torch.zeros(max_batch, dtype=torch.int32, device=dev)
+        self.batch = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.sinks = torch.zeros(Hq, dtype=torch.float32, device=dev)
+
+    def load(self, b):
+        B = b.batch_size
+        q, kv, pt, sk = to_device(b)
+        self.q[:B].copy_(q)
+        self.kv[:b.num_pages].copy_(kv)
+        self.pt[:len(b.page_table)].copy_(pt)
+        self.kv_indptr[:B + 1].copy_(torch.from_numpy(b.kv_indptr))
+        self.lpl[:B].copy_(torch.from_numpy(b.last_page_len))
+        self.batch.fill_(B)
+        self.sinks.copy_(sk)
+        self.out.fill_(float("nan"))
+        self.lse.fill_(float("nan"))
+
+
+def _graph_plan(buf, max_batch, b, **kw):
+    from paged_kv_attention_sink_gb300 import binding
+    return binding.GraphPlan(max_batch, b.num_qo_heads, b.num_kv_heads, b.head_dim, b.page_size, buf.pt,
+                             buf.kv.shape[0], sm_scale=b.sm_scale, **kw)
+
+
+def _decode(plan, buf):
+    return plan.decode(buf.q, buf.kv, buf.kv_indptr, buf.lpl, buf.batch, buf.sinks, buf.out, buf.lse)
+
+
+def _check(b, buf, n=600, seed=0, what=""):
+    rows, heads = sample_pairs(b, list(range(b.batch_size)), n, seed=seed)
+    ref_out, ref_lse = oracle.sink_attention(b, rows=rows, heads=heads)
+    ri = torch.from_numpy(rows).cuda()
+    hi = torch.from_numpy(heads).long().cuda()
+    check_close(buf.out[ri, hi], buf.lse[ri, hi], ref_out, ref_lse, what)
+
+
+def test_device_plan_equals_host_plan():
+    b = syn.gptoss_decode(0)
+    buf = Buffers(96, 64, 8, 64, 16, b.num_pages, len(b.page_table))
+    buf.load(b)
+    plan = _graph_plan(buf, 96, b)
+    _decode(plan, buf)
+    dev_units = plan.device_units()
+    q, kv, pt, sk = to_device(b)
+    host_units = make_plan(b, pt).decode_units()
+    # Same chunks (request, heads, token range, chunk index / count) ...
+    key = lambda u: tuple(int(x) for x in u[:9])
+    assert sorted(map(key, dev_units)) == sorted(map(key, host_units))
+    # ... ordered longest first like the host's ...
+    lens = dev_units[:, 6] - dev_units[:, 5]
+    assert np.all(np.diff(lens) <= 16)            # chunks of one request differ by at most one block
+    # ... and a consistent numbering of split groups and partial slots (the two
+    # planners number them in different orders).
+    groups, slots = {}, set()
+    for u in dev_units:
+        q_row, kv_head, head0, chunk, n_chunks, group, partial0 = (int(u[i]) for i in (0, 2, 3, 7, 8, 9, 10))
+        if n_chunks == 1:
+            assert group == -1
+            continue
+        assert groups.setdefault((q_row, kv_head, head0), (group, partial0)) == (group, partial0)
+        assert partial0 + chunk not in slots
+        slots.add(partial0 + chunk)
+    assert len(set(groups.values())) == len(groups)
+    assert plan.device_error() == 0
+
+
+@pytest.mark.parametrize("which", ["gptoss", "tiny", "long"])
+def test_graph_decode_matches_oracle(which):
+    if which == "gptoss":
+        b = syn.gptoss_decode(3)
+    elif which == "tiny":
+        b = syn.tiny_decode(0)
+    else:
+        b = syn.make_batch("long", [1, 1], [70000, 33], 16, 2, 128, 64, seed=5)
+    buf = Buffers(b.batch_size + 7, b.num_qo_heads, b.num_kv_heads, b.head_dim, b.page_size, b.num_pages,
+                  len(b.page_table))
+    buf.load(b)
+    plan = _graph_plan(buf, b.batch_size + 7, b)
+    _decode(plan, buf)
+    torch.cuda.synchronize()
+    assert plan.device_error() == 0
+    _check(b, buf, what=f"graph decode {which}")
+    assert torch.isnan(buf.out[b.batch_size:].float()).all()      # rows past the batch are not touched
+
+
+def test_cuda_graph_capture_replays_new_batches():
+    """Capture once, replay for three batches of different sizes and lengths."""
+    batches = [syn.gptoss_decode(seed=7, batch=40), syn.gptoss_decode(seed=8, batch=64),
+               syn.make_batch("short", [1] * 9, [5, 17, 300, 1, 16, 64, 2000, 9000, 33], 64, 8, 64, 16, seed=9)]
+    max_pages = max(b.num_pages for b in batches)
+    max_slots = max(len(b.page_table) for b in batches)
+    max_tokens = max(int(b.kv_lens.sum()) for b in batches)
+    buf = Buffers(64, 64, 8, 64, 16, max_pages, max_slots)
+    buf.load(batches[0])
+    plan = _graph_plan(buf, 64, batches[0], max_kv_tokens=max_tokens)
+    _decode(plan, buf)                         # uncaptured call: builds the TMA descriptor
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            _decode(plan, buf)
+    torch.cuda.current_stream().wait_stream(s)
+    for k, b in enumerate(batches):
+        buf.load(b)
+        g.replay()
+        torch.cuda.synchronize()
+        assert plan.device_error() == 0
+        _check(b, buf, n=400, seed=k, what=f"replay {k}")
+
+
+def test_graph_malformed_request_sets_plan_error():
+    b = syn.make_batch("bad", [1, 1, 1], [40, 90, 7], 8, 2, 64, 16, seed=11)
+    buf = Buffers(4, 8, 2, 64, 16, b.num_pages, len(b.page_table))
+    buf.load(b)
+    buf.lpl[1] = 0                              # request 1: last page length out of range
+    plan = _graph_plan(buf, 4, b)
+    _decode(plan, buf)
+    assert plan.device_error() == 4             # ATTN_DEVICE_ERR_PLAN
+    rows = np.array([0, 0, 2, 2]), np.array([0, 5, 1, 7], dtype=np.int32)
+    ref_out, ref_lse = oracle.sink_attention(b, rows=rows[0], heads=rows[1])
+    ri = torch.from_numpy(rows[0]).cuda()
+    hi = torch.from_numpy(rows[1]).long().cuda()
+    check_close(buf.out[ri, hi], buf.lse[ri, hi], ref_out, ref_lse, "graph decode around a bad request")
+    assert torch.isnan(buf.out[1].float()).all()
+
+
+def test_graph_batch_beyond_capacity_sets_plan_error():
+    b = syn.make_batch("cap", [1, 1], [40, 90], 8, 2, 64, 16, seed=12)
+    buf = Buffers(2, 8, 2, 64, 16, b.num_pages, len(b.page_table))
+    buf.load(b)
+    buf.batch.fill_(3)                          # more requests than the plan's max_batch
+    plan = _graph_plan(buf, 2, b)
+    _decode(plan, buf)
+    assert plan.device_error() == 4
