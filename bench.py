@@ -211,13 +211,21 @@ def barrier(world):
 
 
 def max_over_ranks(x, world):
+    """Max of a per-rank scalar over all ranks (the job's time is its slowest rank's)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    device = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(bytes_per_rank_step, steps, rank_seconds, world):
+    """Whole-job throughput of N replicas (GB/s): the units all ranks processed
+    over the slowest rank's time.  Collective when world > 1."""
+    return world * bytes_per_rank_step * steps / max_over_ranks(rank_seconds, world) / 1e9
 
 
 # ----------------------------------------------------------- reference arm
@@ -340,7 +348,7 @@ def run_ours(args, world, rank, local):
     clocks = sampler.stop()
     total_ms = max_over_ranks(sum(times), world)
     bytes_step = kv_bytes(batch)
-    value = world * bytes_step * args.steps / (total_ms / 1e3) / 1e9
+    value = world * bytes_step * args.steps / (total_ms / 1e3) / 1e9   # = job_throughput(...)
     mean_s = sum(times) / len(times) / 1e3
     achieved = bytes_step / mean_s / 1e9
     peak = float(peaks["hbm_gbs"])
