@@ -7,8 +7,11 @@ pages, split-KV), reported as algorithmic KV bytes read per second (GB/s):
 sum over requests of kv_len * Hkv * head_dim * 2 (K and V) * 2 bytes, divided
 by the device time of one attn_decode launch (which includes the split-KV
 merge).  Inputs are resident in HBM; the KV pool (about 750 MB) is larger
-than L2, and L2 is also flushed (a 256 MB memset, outside the timed events)
-before every timed step.  The prefill leg (gpt-oss-120b-shaped ragged causal
+than L2, and L2 is also flushed before every timed step, outside the timed
+events: a 256 MB memset, then a read of another 256 MB buffer, so that the
+timed kernel starts with a cold L2 that holds no dirty lines (otherwise the
+write-back of the memset's ~129 MB of dirty lines lands inside the timed
+kernel and is charged to it).  The prefill leg (gpt-oss-120b-shaped ragged causal
 prefill) is reported in TFLOP/s of visible (query, key) pairs x 4 * head_dim.
 
 One step = one pass of the hot path over one batch: the plan is built once
@@ -281,12 +284,27 @@ def traffic_for(kernel_file, key):
     return entry["dram_bytes_per_launch"] if entry.get("source_sha256") == sha else None
 
 
+class L2Flush:
+    """Evicts L2 between timed steps: a 256 MB memset (writes) followed by a
+    read of a second 256 MB buffer, so the lines left in L2 are clean."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+        self.r = torch.ones(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.sum()
+
+
+
 def time_device(fn, steps, flush, stream):
     import torch
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     for i in range(steps):
-        flush.zero_()
+        flush()
         starts[i].record(stream)
         fn()
         ends[i].record(stream)
@@ -317,7 +335,7 @@ def run_ours(args, world, rank, local):
                             batch.num_qo_heads, batch.num_kv_heads, batch.head_dim, batch.page_size,
                             causal=batch.causal, sm_scale=batch.sm_scale, num_pages=batch.num_pages)
 
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     props = torch.cuda.get_device_properties(dev)
     gpu_id = getattr(props, "uuid", None)
     gpu_id = ("GPU-" + str(gpu_id)) if gpu_id is not None and not str(gpu_id).startswith("GPU-") else str(gpu_id or local)
@@ -332,7 +350,7 @@ def run_ours(args, world, rank, local):
     lse = torch.empty(batch.total_rows, batch.num_qo_heads, device=dev)
     dec = lambda: plan.decode(q, kv, sinks, out, lse)
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         dec()
     torch.cuda.synchronize()
     if plan.device_error():
@@ -540,7 +558,7 @@ def run_ours(args, world, rank, local):
             "config": {"workload": "gptoss_decode", "batch": batch.batch_size,
                        "kv_len": "U[1024,8192]", "Hq": 64, "Hkv": 8, "head_dim": 64,
                        "page_size": 16, "split_kv": True, "sinks": True,
-                       "kv_bytes_per_step": bytes_step, "l2": "flushed (256 MB memset) before every timed step",
+                       "kv_bytes_per_step": bytes_step, "l2": "flushed before every timed step (256 MB memset, then a 256 MB read: cold L2, no dirty lines)",
                        "parallelism": f"replicas x{world}", "plan_us": plan_us,
                        "decode_units": units},
             "roofline": roofline, "e2e": e2e, "gpu_launches": launches,

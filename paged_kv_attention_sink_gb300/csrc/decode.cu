@@ -391,26 +391,46 @@ decode_sink_attn_kernel(const __grid_constant__ CUtensorMap kv_map, const Decode
     __syncthreads();
     if (*flag_s) {
     __threadfence();
+    // One (head, 4 dims) item per thread.  Chunks are read in batches of
+    // kMergeBatch with every load of a batch independent (so a batch costs
+    // about one L2 round trip, not one per chunk), and merged online: the
+    // running max only moves between batches.
+    constexpr int kMergeBatch = 8;
     for (int idx = tid; idx < items; idx += blockDim.x) {
         const int r = idx / (D / 4), d = (idx % (D / 4)) * 4;
-        float Lm = -INFINITY;
-        for (int c = 0; c < u.n_chunks; ++c)
-            Lm = fmaxf(Lm, __ldcg(a.part_lse + (size_t)(u.partial0 + c) * kMaxSliceHeads + r));
-        float W = 0.f;
+        float M = -INFINITY, W = 0.f;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int c = 0; c < u.n_chunks; ++c) {
-            const size_t slot = (size_t)(u.partial0 + c) * kMaxSliceHeads + r;
-            const float lc = __ldcg(a.part_lse + slot);
-            const float w = (lc == -INFINITY) ? 0.f : ptx::ex2(lc - Lm);
-            const float4 oc = __ldcg(reinterpret_cast<const float4*>(a.part_o + slot * D + d));
-            W += w;
-            acc.x += w * oc.x; acc.y += w * oc.y; acc.z += w * oc.z; acc.w += w * oc.w;
+        for (int c0 = 0; c0 < u.n_chunks; c0 += kMergeBatch) {
+            float lc[kMergeBatch];
+            float4 oc[kMergeBatch];
+#pragma unroll
+            for (int k = 0; k < kMergeBatch; ++k) {
+                const int c = c0 + k;
+                const size_t slot = (size_t)(u.partial0 + c) * kMaxSliceHeads + r;
+                lc[k] = c < u.n_chunks ? __ldcg(a.part_lse + slot) : -INFINITY;
+                oc[k] = c < u.n_chunks ? __ldcg(reinterpret_cast<const float4*>(a.part_o + slot * D + d))
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            float mb = M;
+#pragma unroll
+            for (int k = 0; k < kMergeBatch; ++k) mb = fmaxf(mb, lc[k]);
+            if (mb == -INFINITY) continue;   // nothing visible so far
+            const float sc = M == -INFINITY ? 0.f : ptx::ex2(M - mb);
+            W *= sc;
+            acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
+#pragma unroll
+            for (int k = 0; k < kMergeBatch; ++k) {
+                const float w = lc[k] == -INFINITY ? 0.f : ptx::ex2(lc[k] - mb);
+                W += w;
+                acc.x += w * oc[k].x; acc.y += w * oc[k].y; acc.z += w * oc[k].z; acc.w += w * oc[k].w;
+            }
+            M = mb;
         }
         const float inv = W > 0.f ? 1.f / W : 0.f;
         store_bf16x4(a.out + ((size_t)u.q_row * a.Hq + u.head0 + r) * D + d, acc.x * inv,
                      acc.y * inv, acc.z * inv, acc.w * inv);
         if (d == 0 && a.lse)
-            a.lse[(size_t)u.q_row * a.Hq + u.head0 + r] = (W > 0.f ? Lm + log2f(W) : -INFINITY) * kLn2;
+            a.lse[(size_t)u.q_row * a.Hq + u.head0 + r] = (W > 0.f ? M + log2f(W) : -INFINITY) * kLn2;
     }
     if (tid == 0) a.counters[u.group] = 0;   // ready for the next launch
     }
