@@ -59,8 +59,9 @@ bool make_ragged_map(void* map, const void* x, const attn_plan_s* p) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// q [rows][Hq][D] as a 3-D tensor {dim, head, row}: one box is 128 rows x 64
-// dims of one head; rows past the end read as zero.
+// q (or out) [rows][Hq][D] as a 3-D tensor {dim, head, row}: one box is 128
+// rows x 64 dims of one head; rows past the end read as zero (and are not
+// written by a store).
 bool make_q_map(void* map, const void* q, const attn_plan_s* p) {
     auto fn = encode_fn();
     if (!fn) return false;
@@ -177,8 +178,12 @@ extern "C" attn_status attn_prefill(attn_plan_t plan, const void* q, const void*
         if (!make_q_map(plan->q_map_prefill, q, plan)) return ATTN_ERR_CUDA;
         plan->q_map_prefill_ptr = q;
     }
-    return attn::launch_prefill(plan, plan->q_map_prefill, plan->kv_map_prefill, nullptr, sinks, out, lse,
-                                static_cast<cudaStream_t>(stream));
+    if (plan->o_map_prefill_ptr != out) {
+        if (!make_q_map(plan->o_map_prefill, out, plan)) return ATTN_ERR_CUDA;
+        plan->o_map_prefill_ptr = out;
+    }
+    return attn::launch_prefill(plan, plan->q_map_prefill, plan->kv_map_prefill, nullptr, plan->o_map_prefill,
+                                sinks, out, lse, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" attn_status attn_prefill_ragged(attn_plan_t plan, const void* q, const void* k, const void* v,
@@ -201,8 +206,12 @@ extern "C" attn_status attn_prefill_ragged(attn_plan_t plan, const void* q, cons
         if (!make_q_map(plan->q_map_prefill, q, plan)) return ATTN_ERR_CUDA;
         plan->q_map_prefill_ptr = q;
     }
-    return attn::launch_prefill(plan, plan->q_map_prefill, plan->kv_map_prefill, plan->v_map_prefill, sinks, out,
-                                lse, static_cast<cudaStream_t>(stream));
+    if (plan->o_map_prefill_ptr != out) {
+        if (!make_q_map(plan->o_map_prefill, out, plan)) return ATTN_ERR_CUDA;
+        plan->o_map_prefill_ptr = out;
+    }
+    return attn::launch_prefill(plan, plan->q_map_prefill, plan->kv_map_prefill, plan->v_map_prefill,
+                                plan->o_map_prefill, sinks, out, lse, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" attn_status attn_merge_states(const void* va, const float* lsea, const void* vb,

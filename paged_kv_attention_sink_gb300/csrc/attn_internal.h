@@ -100,4 +100,6 @@ struct attn_plan_s {
     const void* q_map_prefill_ptr = nullptr;
     alignas(64) unsigned char v_map_prefill[128];   // ragged: K in kv_map_prefill, V here
     const void* v_map_prefill_ptr = nullptr;
+    alignas(64) unsigned char o_map_prefill[128];   // out, laid out like q
+    const void* o_map_prefill_ptr = nullptr;
 };

@@ -10,9 +10,11 @@ namespace attn {
 // kv_map / q_map point at CUtensorMap objects built by the API layer.
 attn_status launch_decode(attn_plan_s* plan, const void* q, const void* kv_map, const float* sinks,
                           void* out, float* lse, cudaStream_t stream);
-// v_map: the V tensor map of a ragged plan (NULL for a paged plan).
+// v_map: the V tensor map of a ragged plan (NULL for a paged plan); o_map:
+// `out` with the same layout and box as q_map (full 128-row tiles are stored
+// through it).
 attn_status launch_prefill(attn_plan_s* plan, const void* q_map, const void* kv_map, const void* v_map,
-                           const float* sinks, void* out, float* lse, cudaStream_t stream);
+                           const void* o_map, const float* sinks, void* out, float* lse, cudaStream_t stream);
 attn_status launch_merge_states(const void* va, const float* lsea, const void* vb,
                                 const float* lseb, void* vout, float* lseout, int64_t rows,
                                 int head_dim, cudaStream_t stream);

@@ -77,7 +77,7 @@ struct PrefillCfg {
     static constexpr int kOffPb = kOffV + kStagesV * kTile;                 // per head 128 rows x 128 B
     static constexpr int kOffOnes = kOffPb + (kSplitP ? 2 * kAtom : 0);     // 16 key rows x 128 B
     static constexpr int kOffBar = kOffOnes + (kSplitP ? 2048 : 0);
-    static constexpr int kNumBars = 2 * kQBufs + 2 * kStagesK + 2 * kStagesV + 8 + 2 + 8;
+    static constexpr int kNumBars = 2 * kQBufs + 2 * kStagesK + 2 * kStagesV + 8 + 2 + 8 + 4;
     static constexpr int kSmem = 1024 + kOffBar + kNumBars * 8 + 16;
     static constexpr uint32_t kTmemCols = 512;
     // TMEM columns of head slot i (every region starts on a multiple of 32).
@@ -102,7 +102,7 @@ struct PrefillArgs {
 
 struct Bars {
     uint32_t q_full, q_empty, k_full, k_empty, v_full, v_empty, s_full, s_free, p_full, o_done,
-        v_aux, drain, turn;
+        v_aux, drain, turn, o_staged, o_free;
 };
 
 // Warp-uniform bounded wait.
@@ -117,7 +117,8 @@ template <int D, bool kRagged>
 __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
 prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                          const __grid_constant__ CUtensorMap kv_map,
-                         const __grid_constant__ CUtensorMap v_map, const PrefillArgs a) {
+                         const __grid_constant__ CUtensorMap v_map,
+                         const __grid_constant__ CUtensorMap o_map, const PrefillArgs a) {
     using C = PrefillCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -141,6 +142,8 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
     B.v_aux = B.o_done + 16;
     B.drain = B.v_aux + 8;
     B.turn = B.drain + 8;   // [quadrant][head slot]
+    B.o_staged = B.turn + 64;   // [head slot]: the 4 warps' output rows are in shared memory
+    B.o_free = B.o_staged + 16; // [head slot]: the output store has read them
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int item_begin = a.item_off[blockIdx.x], item_end = a.item_off[blockIdx.x + 1];
@@ -169,9 +172,14 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
         ptx::mbar_init(B.v_aux, 1);
         ptx::mbar_init(B.drain, 2);
         for (int k = 0; k < 8; ++k) ptx::mbar_init(B.turn + 8 * k, 1);
+        for (int k = 0; k < 2; ++k) {
+            ptx::mbar_init(B.o_staged + 8 * k, 4);
+            ptx::mbar_init(B.o_free + 8 * k, 1);
+        }
         *abort_flag = 0;
         ptx::prefetch_tmap(&q_map);
         ptx::prefetch_tmap(&kv_map);
+        ptx::prefetch_tmap(&o_map);
         ptx::fence_mbar_init();
     }
     if (warp == 1) {
@@ -465,6 +473,15 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
         // waits and stores.  Head slot 0 goes first.
         const uint32_t my_turn = B.turn + 8 * (quad * 2 + i), other_turn = B.turn + 8 * (quad * 2 + (i ^ 1));
         int n_turn = 0;
+        // D = 64: a full 128-row tile's output leaves through the P buffer of
+        // this head slot and one TMA store (rows one thread apart are 8 KB
+        // apart in `out`, so per-thread stores would touch 32 lines per
+        // instruction).  The buffer is reused for the next item's P only
+        // after the store has read it.
+        const uint32_t pb_base = sbase + C::kOffPb + i * C::kAtom;
+        const bool o_leader = (tid & 127) == 0;   // thread 0 of this head slot's warpgroup
+        bool o_pending = false;
+        int n_ostore = 0;
         if (i == 1 && lane == 0) ptx::mbar_arrive(other_turn);
         for (int item = item_begin; ok && item < item_end; ++item) {
             const PrefillItem it = a.items[item];
@@ -605,6 +622,15 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                     if (!wait_all(B.o_done + 8 * i, (t - 1) & 1)) { ok = false; break; }
                     ptx::tc_fence_after();
                 }
+                if (C::kSplitP && o_pending) {
+                    // The previous item's output store must have read the buffer.
+                    if (o_leader) {
+                        ptx::bulk_wait_read_all();
+                        ptx::mbar_arrive(B.o_free + 8 * i);
+                    }
+                    if (!wait_all(B.o_free + 8 * i, (n_ostore - 1) & 1)) { ok = false; break; }
+                    o_pending = false;
+                }
                 ptx::tmem_st32(t_p, pk[0]);
                 if constexpr (C::kSplitP) {
 #pragma unroll
@@ -634,6 +660,39 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const bool store = r < it.n_rows;
             __nv_bfloat16* orow = a.out + ((size_t)(it.q_row0 + r) * a.Hq + head) * D;
+            if (C::kSplitP && it.n_rows == kPrefillRows) {
+                // Row r of O, normalised and rounded, into the P buffer with the
+                // out tensor map's 128-byte swizzle; then one TMA store.
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t v[32];
+                    ptx::tmem_ld32(t_o + c * 32, v);
+                    ptx::tc_wait_ld();
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int e = 8 * q;
+                        ptx::st_shared_v4(
+                            pb_row + (((c * 4 + q) ^ (r & 7)) << 4),
+                            ptx::pack_bf16x2(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv),
+                            ptx::pack_bf16x2(__uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv),
+                            ptx::pack_bf16x2(__uint_as_float(v[e + 4]) * inv, __uint_as_float(v[e + 5]) * inv),
+                            ptx::pack_bf16x2(__uint_as_float(v[e + 6]) * inv, __uint_as_float(v[e + 7]) * inv));
+                    }
+                }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(B.o_staged + 8 * i);
+                if ((tid & 127) < 32) {   // the leader's warp waits for all four
+                    if (!wait_all(B.o_staged + 8 * i, n_ostore & 1)) {
+                        ok = false;
+                    } else if (o_leader) {
+                        ptx::tma_store_3d(&o_map, pb_base, 0, head, it.q_row0);
+                        ptx::bulk_commit_group();
+                    }
+                }
+                o_pending = true;
+                ++n_ostore;
+            } else {
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t v[32];
@@ -651,11 +710,13 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                     }
                 }
             }
+            }
             if (store && a.lse)
                 a.lse[(size_t)(it.q_row0 + r) * a.Hq + head] =
                     le > 0.f ? (m_use + log2f(le)) * kLn2 : -INFINITY;
         }
         if (!ok) fail(ATTN_DEVICE_ERR_TIMEOUT);
+        if (o_leader) ptx::bulk_wait_all();   // output stores complete before the CTA exits
     }
 
     // Tear-down: each MMA thread's last commit arrives on `drain` once every
@@ -671,8 +732,8 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
 }
 
 template <int D, bool kRagged>
-cudaError_t launch(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm, const PrefillArgs& args,
-                   int grid, cudaStream_t stream) {
+cudaError_t launch(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm, const CUtensorMap& om,
+                   const PrefillArgs& args, int grid, cudaStream_t stream) {
     using C = PrefillCfg<D>;
     auto kernel = prefill_sink_attn_kernel<D, kRagged>;
     static bool configured = false;
@@ -686,14 +747,14 @@ cudaError_t launch(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorM
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    kernel<<<grid, C::kThreads, C::kSmem, stream>>>(qm, km, vm, args);
+    kernel<<<grid, C::kThreads, C::kSmem, stream>>>(qm, km, vm, om, args);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 attn_status launch_prefill(attn_plan_s* plan, const void* q_map, const void* kv_map, const void* v_map,
-                           const float* sinks, void* out, float* lse, cudaStream_t stream) {
+                           const void* o_map, const float* sinks, void* out, float* lse, cudaStream_t stream) {
     if (plan->items.empty()) return ATTN_OK;
     PrefillArgs a;
     a.items = reinterpret_cast<const PrefillItem*>(plan->ws + plan->layout.items);
@@ -712,15 +773,17 @@ attn_status launch_prefill(attn_plan_s* plan, const void* q_map, const void* kv_
     const CUtensorMap& qm = *static_cast<const CUtensorMap*>(q_map);
     const CUtensorMap& km = *static_cast<const CUtensorMap*>(kv_map);
     const CUtensorMap& vm = *static_cast<const CUtensorMap*>(v_map ? v_map : kv_map);
+    const CUtensorMap& om = *static_cast<const CUtensorMap*>(o_map);
     // Persistent grid: one CTA per planned item list (at most one per SM; the
     // kernel holds all of an SM's TMEM).
     const int grid = plan->prefill_ctas;
     cudaError_t e;
     if (plan->ragged)
-        e = plan->D == 64 ? launch<64, true>(qm, km, vm, a, grid, stream) : launch<128, true>(qm, km, vm, a, grid, stream);
+        e = plan->D == 64 ? launch<64, true>(qm, km, vm, om, a, grid, stream)
+                          : launch<128, true>(qm, km, vm, om, a, grid, stream);
     else
-        e = plan->D == 64 ? launch<64, false>(qm, km, vm, a, grid, stream)
-                          : launch<128, false>(qm, km, vm, a, grid, stream);
+        e = plan->D == 64 ? launch<64, false>(qm, km, vm, om, a, grid, stream)
+                          : launch<128, false>(qm, km, vm, om, a, grid, stream);
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
