@@ -202,6 +202,7 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+
     auto fail = [&](int code) {
         atomicOr(a.err, code);
         *abort_flag = 1;
@@ -397,13 +398,23 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
         auto kfull = [&](int t) { return wait_all(B.k_full + 8 * (t % C::kStagesK), (t / C::kStagesK) & 1); };
         auto vfull = [&](int t) { return wait_all(B.v_full + 8 * (t % C::kStagesV), (t / C::kStagesV) & 1); };
 
+        // The next item's tile and head counts are loaded one item ahead, so
+        // their global load never sits between two items' MMAs.
+        int nx_tiles = 0, nx_heads = 0;
+        if (item_begin < item_end) {
+            nx_tiles = a.items[item_begin].n_kv_tiles;
+            nx_heads = a.items[item_begin].n_heads;
+        }
         for (int item = item_begin; ok && item < item_end; ++item, ++n_item) {
             if (*abort_flag) { ok = false; break; }
-            const PrefillItem it = a.items[item];
-            const int n = it.n_kv_tiles;
+            const int n = nx_tiles, n_heads = nx_heads;
+            if (item + 1 < item_end) {
+                nx_tiles = a.items[item + 1].n_kv_tiles;
+                nx_heads = a.items[item + 1].n_heads;
+            }
             const int qb = n_item % C::kQBufs;
             if (!wait_all(B.q_full + 8 * qb, (n_item / C::kQBufs) & 1)) { ok = false; break; }
-            if (i >= it.n_heads) {
+            if (i >= n_heads) {
                 // This head slot has no work in the item: only keep the
                 // shared stages' arrival counts (after each stage is loaded).
                 for (int j = 0; j < n && ok; ++j) {
@@ -483,6 +494,10 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
         bool o_pending = false;
         int n_ostore = 0;
         if (i == 1 && lane == 0) ptx::mbar_arrive(other_turn);
+        // Item descriptors and sinks are read from L1: the sinks' lines are
+        // prefetched here, each next descriptor after the current item's last
+        // tile (its latency then overlaps the wait for the last PV).
+        if (a.sinks != nullptr && lane * 32 < a.Hq) ptx::prefetch_l1(a.sinks + lane * 32);
         for (int item = item_begin; ok && item < item_end; ++item) {
             const PrefillItem it = a.items[item];
             if (i >= it.n_heads) continue;
@@ -647,6 +662,8 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                 if (lane == 0) ptx::mbar_arrive(B.p_full + 8 * i);
             }
             if (!ok) break;
+            if (item + 1 < item_end && lane < 2)   // a descriptor may straddle two lines
+                ptx::prefetch_l1(reinterpret_cast<const char*>(a.items + item + 1) + lane * (sizeof(PrefillItem) - 1));
             // Epilogue: O of this item is complete once the last PV is done.
             if (!wait_all(B.o_done + 8 * i, (hj + n - 1) & 1)) { ok = false; break; }
             ptx::tc_fence_after();
