@@ -96,20 +96,20 @@ extern "C" attn_status attn_plan_bind_workspace(attn_plan_t plan, void* workspac
     if (bytes < L.total) return ATTN_ERR_WORKSPACE_TOO_SMALL;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     unsigned char* ws = static_cast<unsigned char*>(workspace);
-    if (!plan->units.empty() &&
-        cudaMemcpyAsync(ws + L.units, plan->units.data(), plan->units.size() * sizeof(attn::DecodeUnit),
-                        cudaMemcpyHostToDevice, s) != cudaSuccess)
-        return ATTN_ERR_CUDA;
-    if (!plan->items.empty() &&
-        (cudaMemcpyAsync(ws + L.items, plan->items.data(), plan->items.size() * sizeof(attn::PrefillItem),
-                         cudaMemcpyHostToDevice, s) != cudaSuccess ||
-         cudaMemcpyAsync(ws + L.item_off, plan->item_off.data(), plan->item_off.size() * sizeof(int32_t),
-                         cudaMemcpyHostToDevice, s) != cudaSuccess))
-        return ATTN_ERR_CUDA;
-    if (!plan->append_slots.empty() &&
-        cudaMemcpyAsync(ws + L.append, plan->append_slots.data(), plan->append_slots.size() * sizeof(int32_t),
-                        cudaMemcpyHostToDevice, s) != cudaSuccess)
-        return ATTN_ERR_CUDA;
+    // The work lists lie in [0, L.counters): one host image, one copy (graph
+    // plans have none: their list is built on the device).
+    if (!plan->units.empty() || !plan->items.empty() || !plan->append_slots.empty()) {
+        std::vector<unsigned char> img(L.counters, 0);
+        auto put = [&](size_t off, const void* src, size_t bytes) {
+            if (bytes) std::memcpy(img.data() + off, src, bytes);
+        };
+        put(L.units, plan->units.data(), plan->units.size() * sizeof(attn::DecodeUnit));
+        put(L.items, plan->items.data(), plan->items.size() * sizeof(attn::PrefillItem));
+        put(L.item_off, plan->item_off.data(), plan->item_off.size() * sizeof(int32_t));
+        put(L.append, plan->append_slots.data(), plan->append_slots.size() * sizeof(int32_t));
+        if (cudaMemcpyAsync(ws, img.data(), img.size(), cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+    }
     // counters and the error word are adjacent: clear both.
     if (cudaMemsetAsync(ws + L.counters, 0, L.part_lse - L.counters, s) != cudaSuccess) return ATTN_ERR_CUDA;
     plan->ws = ws;

@@ -117,42 +117,60 @@ attn_status make_plan(bool ragged, const int32_t* qo_indptr, const int32_t* kv_i
     int64_t chunk = (total_blocks + target_units - 1) / target_units;
     chunk = std::min<int64_t>(std::max<int64_t>(chunk, kDecodeMinChunkBlocks), kDecodeMaxChunkBlocks);
 
+    // Chunks of each request (every KV head and head slice of a request has
+    // the same chunks): [c * nblk / n, (c + 1) * nblk / n) blocks.  Split
+    // groups are numbered in (request, KV head, slice) order, each group's
+    // partial slots contiguous.
+    struct Piece { int32_t b, c, n, t0, t1, group0, partial0; };
+    std::vector<Piece> pieces;
+    pieces.reserve((size_t)n_decode * 4);
+    const int32_t per_request = num_kv_heads * n_slices;   // (KV head, slice) pairs
     for (int32_t b = 0; b < batch; ++b) {
         if (qo_len[b] != 1 || ragged) continue;
         const int64_t nblk = (kv_len[b] + kBlockTokens - 1) / kBlockTokens;
         int64_t n_chunks = std::max<int64_t>(1, (nblk + chunk / 2) / chunk);
         n_chunks = std::max<int64_t>(n_chunks, (nblk + kDecodeMaxChunkBlocks - 1) / kDecodeMaxChunkBlocks);
-        for (int32_t g = 0; g < num_kv_heads; ++g) {
-            for (int s = 0; s < n_slices; ++s) {
-                int32_t group = -1, partial0 = 0;
-                if (n_chunks > 1) {
-                    group = plan->n_groups++;
-                    partial0 = plan->n_partials;
-                    plan->n_partials += (int32_t)n_chunks;
+        int32_t group0 = -1, partial0 = 0;
+        if (n_chunks > 1) {
+            group0 = plan->n_groups;
+            partial0 = plan->n_partials;
+            plan->n_groups += per_request;
+            plan->n_partials += per_request * (int32_t)n_chunks;
+        }
+        for (int64_t c = 0; c < n_chunks; ++c) {
+            const int64_t blk0 = c * nblk / n_chunks, blk1 = (c + 1) * nblk / n_chunks;
+            pieces.push_back({b, (int32_t)c, (int32_t)n_chunks, (int32_t)(blk0 * kBlockTokens),
+                              (int32_t)std::min<int64_t>(kv_len[b], blk1 * kBlockTokens), group0, partial0});
+        }
+    }
+    // Longest first (equal lengths keep request order), then every (KV head,
+    // slice) of a chunk in turn.
+    std::stable_sort(pieces.begin(), pieces.end(),
+                     [](const Piece& x, const Piece& y) { return (x.t1 - x.t0) > (y.t1 - y.t0); });
+    plan->units.resize(pieces.size() * (size_t)per_request);
+    DecodeUnit* out = plan->units.data();
+    for (const Piece& pc : pieces) {
+        DecodeUnit u{};
+        u.q_row = qo_indptr[pc.b];
+        u.page_base = kv_indptr[pc.b];
+        u.tok_begin = pc.t0;
+        u.tok_end = pc.t1;
+        u.chunk = pc.c;
+        u.n_chunks = pc.n;
+        u.group = -1;
+        for (int32_t g = 0, k = 0; g < num_kv_heads; ++g) {
+            for (int32_t sl = 0; sl < n_slices; ++sl, ++k) {
+                u.kv_head = g;
+                u.head0 = g * G + sl * kMaxSliceHeads;
+                u.n_heads = std::min(kMaxSliceHeads, G - sl * kMaxSliceHeads);
+                if (pc.n > 1) {
+                    u.group = pc.group0 + k;
+                    u.partial0 = pc.partial0 + k * pc.n;
                 }
-                for (int64_t c = 0; c < n_chunks; ++c) {
-                    const int64_t blk0 = c * nblk / n_chunks, blk1 = (c + 1) * nblk / n_chunks;
-                    DecodeUnit u{};
-                    u.q_row = qo_indptr[b];
-                    u.page_base = kv_indptr[b];
-                    u.kv_head = g;
-                    u.head0 = g * G + s * kMaxSliceHeads;
-                    u.n_heads = std::min(kMaxSliceHeads, G - s * kMaxSliceHeads);
-                    u.tok_begin = (int32_t)(blk0 * kBlockTokens);
-                    u.tok_end = (int32_t)std::min<int64_t>(kv_len[b], blk1 * kBlockTokens);
-                    u.chunk = (int32_t)c;
-                    u.n_chunks = (int32_t)n_chunks;
-                    u.group = group;
-                    u.partial0 = partial0;
-                    plan->units.push_back(u);
-                }
+                *out++ = u;
             }
         }
     }
-    std::stable_sort(plan->units.begin(), plan->units.end(),
-                     [](const DecodeUnit& a, const DecodeUnit& b) {
-                         return (a.tok_end - a.tok_begin) > (b.tok_end - b.tok_begin);
-                     });
 
     // ---- prefill: one item per (128-row tile, pair of query heads of a group),
     // visiting 128-key KV tiles up to the causal diagonal.
