@@ -18,7 +18,8 @@ One step = one pass of the hot path over one batch: the plan is built once
 per batch (host), then attn_decode runs (and attn_prefill for the prefill
 leg).  `e2e` times the same decode through the public API from pinned host
 buffers: H2D of q and the page table, planning and work-list upload, the
-launch, and D2H of out and lse, every step.
+launch, and D2H of out and lse, every step, with two steps in flight (the
+host plans step k while the GPU runs step k-1).
 
 Multi-GPU: the path shards by request with no exchange, so N ranks run N
 independent replicas ("scaling": "weak"); value = all ranks' bytes / max
@@ -408,38 +409,51 @@ def run_ours(args, world, rank, local):
     except binding.AttnError as e:
         graph = {"unavailable": str(e)}
 
-    # ---- e2e through the public API from pinned host buffers
+    # ---- e2e through the public API from pinned host buffers.  Two steps are
+    # in flight, as a serving loop would run them: the host plans and launches
+    # step k (H2D of its q and page table, attn_plan + workspace upload,
+    # attn_decode, D2H of its out and lse) while the GPU still runs step k-1,
+    # and waits for a step's read-back before reusing its buffers.
     q_h = torch.from_numpy(batch.q.view(np.int16)).view(torch.bfloat16).pin_memory()
     pt_h = torch.from_numpy(batch.page_table).pin_memory()
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    q_d = torch.empty_like(q)
-    pt_d = torch.empty_like(pt)
+    e2e_slots = []
+    for _ in range(2):
+        e2e_slots.append({
+            "q": torch.empty_like(q), "pt": torch.empty_like(pt), "out": torch.empty_like(out),
+            "lse": torch.empty_like(lse), "out_h": torch.empty(out.shape, dtype=out.dtype).pin_memory(),
+            "lse_h": torch.empty(lse.shape, dtype=lse.dtype).pin_memory(), "ev": torch.cuda.Event(),
+            "plan": None})
     e2e_steps = max(3, min(args.steps, 200))
 
-    def e2e_step():
-        q_d.copy_(q_h, non_blocking=True)
-        pt_d.copy_(pt_h, non_blocking=True)
-        p = plan_of(batch, pt_d)
-        p.decode(q_d, kv, sinks, out, lse)
-        out_h.copy_(out, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
-        torch.cuda.synchronize()
-        return p
+    def e2e_step(k):
+        sl = e2e_slots[k % 2]
+        if sl["plan"] is not None:
+            sl["ev"].synchronize()   # step k-2's result is on the host; its buffers are free
+        sl["q"].copy_(q_h, non_blocking=True)
+        sl["pt"].copy_(pt_h, non_blocking=True)
+        sl["plan"] = plan_of(batch, sl["pt"])
+        sl["plan"].decode(sl["q"], kv, sinks, sl["out"], sl["lse"])
+        sl["out_h"].copy_(sl["out"], non_blocking=True)
+        sl["lse_h"].copy_(sl["lse"], non_blocking=True)
+        sl["ev"].record()
 
-    for _ in range(3):
-        e2e_step()
+    for k in range(3):
+        e2e_step(k)
+    torch.cuda.synchronize()
     barrier(world)
     t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        e2e_step()
+    for k in range(e2e_steps):
+        e2e_step(k)
+    torch.cuda.synchronize()
     e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    if not torch.equal(e2e_slots[0]["out_h"].view(torch.int16), e2e_slots[1]["out_h"].view(torch.int16)):
+        raise RuntimeError("end-to-end decode steps on the same batch disagree")
     units = plan.info()["num_decode_units"]
     h2d = q_h.numel() * 2 + pt_h.numel() * 4 + units * 48
-    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+    d2h = e2e_slots[0]["out_h"].numel() * 2 + e2e_slots[0]["lse_h"].numel() * 4
     e2e = {"value": world * bytes_step * e2e_steps / e2e_s / 1e9, "unit": "GB/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "ms_per_step": e2e_s * 1e3 / e2e_steps}
+           "ms_per_step": e2e_s * 1e3 / e2e_steps, "steps_in_flight": 2}
 
     # ---- prefill leg (TFLOP/s), if the kernel is available
     prefill = None
