@@ -548,6 +548,76 @@ def run_ours(args, world, rank, local):
         }
         launches += 2 * asteps
 
+    # ---- the other serving shapes: Qwen3-shaped long-context decode (no
+    # sinks) and the mixed batch (chunked prefill on cached prefixes + 256
+    # decode requests, one plan, prefill then decode on one stream).
+    others = None
+    if not args.no_prefill and prefill is not None and "unavailable" not in prefill:
+        others = {}
+        hbm = float(peaks["hbm_gbs"])
+        tc = float(peaks["bf16_tflops"])
+        osteps = max(3, args.steps // 10)
+        def pool_on_device(b_):
+            # N(0,1) bf16, drawn on the GPU (seeded): these legs only time kernels
+            g = torch.Generator(device=dev)
+            g.manual_seed(1000 + rank)
+            pool = torch.empty((b_.num_pages, 2, b_.num_kv_heads, b_.page_size, b_.head_dim), dtype=torch.bfloat16,
+                               device=dev)
+            flat = pool.view(-1)
+            for s0 in range(0, flat.numel(), 1 << 28):
+                n = min(1 << 28, flat.numel() - s0)
+                flat[s0:s0 + n] = torch.randn(n, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+            return pool
+
+        def to_dev_gen(b_):
+            q_ = torch.from_numpy(b_.q.view(np.int16)).view(torch.bfloat16).to(dev)
+            pt_ = torch.from_numpy(b_.page_table).to(dev)
+            sk_ = None if b_.sinks is None else torch.from_numpy(b_.sinks).to(dev)
+            return q_, pool_on_device(b_), pt_, sk_
+
+        qb = syn.qwen_decode(seed=rank, fill_pool=False)
+        qq, qkv, qpt, qsk = to_dev_gen(qb)
+        qplan = plan_of(qb, qpt)
+        qout = torch.empty_like(qq)
+        qlse = torch.empty(qb.total_rows, qb.num_qo_heads, device=dev)
+        qdec = lambda: qplan.decode(qq, qkv, qsk, qout, qlse)
+        for _ in range(args.warmup):
+            qdec()
+        qtimes = time_device(qdec, osteps, flush, stream)
+        qmean = sum(qtimes) / len(qtimes) / 1e3
+        qbytes = kv_bytes(qb)
+        others["qwen_decode"] = {
+            "workload": "qwen_decode: 128 requests, kv_len log-U[2048,32768], Hq 64, Hkv 4, D 128, P 64, no sinks"
+                        " (KV pool drawn on the GPU)",
+            "bytes": qbytes, "ms_per_step": qmean * 1e3, "value": qbytes / qmean / 1e9, "unit": "GB/s",
+            "frac_of_hbm_peak": qbytes / qmean / 1e9 / hbm}
+        launches += osteps
+        del qq, qkv, qpt, qout, qlse, qplan
+        mb = syn.mixed(seed=rank, fill_pool=False)
+        mq, mkv, mpt, msk = to_dev_gen(mb)
+        mplan = plan_of(mb, mpt)
+        mout = torch.empty_like(mq)
+        mlse = torch.empty(mb.total_rows, mb.num_qo_heads, device=dev)
+        mpre = lambda: mplan.prefill(mq, mkv, msk, mout, mlse)
+        mdec = lambda: mplan.decode(mq, mkv, msk, mout, mlse)
+        for _ in range(args.warmup):
+            mpre()
+            mdec()
+        mp = time_device(mpre, osteps, flush, stream)
+        md = time_device(mdec, osteps, flush, stream)
+        mboth = time_device(lambda: (mpre(), mdec()), osteps, flush, stream)
+        mp_s, md_s, mb_s = (sum(t) / len(t) / 1e3 for t in (mp, md, mboth))
+        mflops, mbytes = prefill_flops(mb), kv_bytes(mb)
+        ideal = mflops / (tc * 1e12) + mbytes / (hbm * 1e9)
+        others["mixed"] = {
+            "workload": "mixed: 4 prefills (qo 2048 on prefixes 0/2048/4096/8192) + 256 decodes (kv U[512,16384])"
+                        " (KV pool drawn on the GPU)",
+            "prefill_tflops": mflops / mp_s / 1e12, "prefill_frac_of_bf16_peak": mflops / mp_s / 1e12 / tc,
+            "decode_gbs": mbytes / md_s / 1e9, "decode_frac_of_hbm_peak": mbytes / md_s / 1e9 / hbm,
+            "both_ms": mb_s * 1e3, "combined_frac_of_ideal": ideal / mb_s}
+        launches += 4 * osteps
+        del mq, mkv, mpt, mout, mlse, mplan
+
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -577,6 +647,7 @@ def run_ours(args, world, rank, local):
                        "decode_units": units},
             "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
             "clocks": clocks, "cpu_baseline": cpu, "decode_graph": graph, "prefill": prefill, "prefill_ragged": ragged, "kv_cache": kvcache,
+            "other_shapes": others,
         }
         print(json.dumps(line), flush=True)
 

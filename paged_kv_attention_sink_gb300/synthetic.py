@@ -63,8 +63,9 @@ class Batch:
     page_table: np.ndarray     # [kv_indptr[B]] int32
     last_page_len: np.ndarray  # [B] int32
     q: np.ndarray              # [rows, Hq, D] uint16 (bf16 bits)
-    kv_pool: np.ndarray        # [num_pages, 2, Hkv, P, D] uint16 (bf16 bits)
+    kv_pool: Optional[np.ndarray]  # [num_pages, 2, Hkv, P, D] uint16 (bf16 bits); None if not drawn
     sinks: Optional[np.ndarray]  # [Hq] float32 or None
+    pool_pages: int = 0        # pages in the pool (also when kv_pool is None)
 
     @property
     def batch_size(self) -> int:
@@ -72,7 +73,7 @@ class Batch:
 
     @property
     def num_pages(self) -> int:
-        return self.kv_pool.shape[0]
+        return self.kv_pool.shape[0] if self.kv_pool is not None else self.pool_pages
 
     @property
     def total_rows(self) -> int:
@@ -91,8 +92,10 @@ def make_batch(name: str, qo_lens: Sequence[int], kv_lens: Sequence[int], num_qo
                num_kv_heads: int, head_dim: int, page_size: int, *, causal: bool = True,
                with_sinks: bool = True, pool_pages: Optional[int] = None,
                pool_factor: float = 1.25, rng: Optional[np.random.Generator] = None,
-               seed: int = 0) -> Batch:
-    """Lay out one ragged batch (see the module docstring for the recipe)."""
+               seed: int = 0, fill_pool: bool = True) -> Batch:
+    """Lay out one ragged batch (see the module docstring for the recipe).
+    fill_pool=False leaves kv_pool as None (a caller that only times kernels
+    draws the pool on the device itself)."""
     if rng is None:
         rng = np.random.Generator(np.random.PCG64(seed))
     qo = np.asarray(qo_lens, dtype=np.int64)
@@ -112,19 +115,21 @@ def make_batch(name: str, qo_lens: Sequence[int], kv_lens: Sequence[int], num_qo
     last_page_len = np.where(n_pages > 0, kv - (n_pages - 1) * P, 0).astype(np.int32)
 
     q = _normal_bf16(rng, int(qo.sum()) * Hq * D).reshape(int(qo.sum()), Hq, D)
-    kv_pool = _normal_bf16(rng, pool * 2 * Hkv * P * D).reshape(pool, 2, Hkv, P, D)
-    used = np.zeros(pool, dtype=bool)
-    used[page_table] = True
-    kv_pool[~used] = BF16_NAN
-    for b in range(B):
-        if n_pages[b] > 0 and last_page_len[b] < P:
-            last = page_table[kv_indptr[b + 1] - 1]
-            kv_pool[last, :, :, last_page_len[b]:, :] = BF16_NAN
+    kv_pool = None
+    if fill_pool:
+        kv_pool = _normal_bf16(rng, pool * 2 * Hkv * P * D).reshape(pool, 2, Hkv, P, D)
+        used = np.zeros(pool, dtype=bool)
+        used[page_table] = True
+        kv_pool[~used] = BF16_NAN
+        for b in range(B):
+            if n_pages[b] > 0 and last_page_len[b] < P:
+                last = page_table[kv_indptr[b + 1] - 1]
+                kv_pool[last, :, :, last_page_len[b]:, :] = BF16_NAN
     sinks = rng.standard_normal(Hq, dtype=np.float32) if with_sinks else None
     return Batch(name=name, num_qo_heads=Hq, num_kv_heads=Hkv, head_dim=D, page_size=P,
                  causal=causal, sm_scale=1.0 / math.sqrt(D), qo_lens=qo, kv_lens=kv,
                  qo_indptr=qo_indptr, kv_indptr=kv_indptr, page_table=page_table,
-                 last_page_len=last_page_len, q=q, kv_pool=kv_pool, sinks=sinks)
+                 last_page_len=last_page_len, q=q, kv_pool=kv_pool, sinks=sinks, pool_pages=pool)
 
 
 def _rng(seed: int) -> np.random.Generator:
@@ -152,16 +157,17 @@ def gptoss_prefill(seed: int = 0, n_seq: int = 8) -> Batch:
     return make_batch("gptoss_prefill", L, L, 64, 8, 64, 16, causal=True, rng=rng)
 
 
-def qwen_decode(seed: int = 0, batch: int = 128) -> Batch:
+def qwen_decode(seed: int = 0, batch: int = 128, fill_pool: bool = True) -> Batch:
     """Qwen3-235B-shaped long-context decode without sinks: kv_len log-uniform in
     [2048, 32768], Hq 64 / Hkv 4, D 128, 64-token pages."""
     rng = _rng(seed)
     kv = np.exp(rng.uniform(math.log(2048), math.log(32768), size=batch))
     kv = np.clip(np.rint(kv), 2048, 32768).astype(np.int64)
-    return make_batch("qwen_decode", [1] * batch, kv, 64, 4, 128, 64, with_sinks=False, rng=rng)
+    return make_batch("qwen_decode", [1] * batch, kv, 64, 4, 128, 64, with_sinks=False, rng=rng,
+                      fill_pool=fill_pool)
 
 
-def mixed(seed: int = 0, n_decode: int = 256) -> Batch:
+def mixed(seed: int = 0, n_decode: int = 256, fill_pool: bool = True) -> Batch:
     """Mixed serving batch: 4 chunked-prefill requests (qo_len 2048 on cached
     prefixes of 0 / 2048 / 4096 / 8192 tokens, causal) followed by decode
     requests with kv_len ~ U[512, 16384]; Hq 64 / Hkv 8, D 64, P 16."""
@@ -170,7 +176,7 @@ def mixed(seed: int = 0, n_decode: int = 256) -> Batch:
     dec_kv = rng.integers(512, 16384, size=n_decode, endpoint=True)
     qo = np.concatenate([np.full(4, 2048), np.ones(n_decode, dtype=np.int64)])
     kv = np.concatenate([prefix + 2048, dec_kv])
-    return make_batch("mixed", qo, kv, 64, 8, 64, 16, causal=True, rng=rng)
+    return make_batch("mixed", qo, kv, 64, 8, 64, 16, causal=True, rng=rng, fill_pool=fill_pool)
 
 
 WORKLOADS = {
