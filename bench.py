@@ -331,10 +331,11 @@ def run_ours(args, world, rank, local):
         sk = None if batch.sinks is None else torch.from_numpy(batch.sinks).to(dev)
         return q, kv, pt, sk
 
-    def plan_of(batch, pt):
+    def plan_of(batch, pt, workspace=None):
         return binding.Plan(batch.qo_indptr, batch.kv_indptr, pt, batch.last_page_len,
                             batch.num_qo_heads, batch.num_kv_heads, batch.head_dim, batch.page_size,
-                            causal=batch.causal, sm_scale=batch.sm_scale, num_pages=batch.num_pages)
+                            causal=batch.causal, sm_scale=batch.sm_scale, num_pages=batch.num_pages,
+                            workspace=workspace)
 
     flush = L2Flush(dev)
     props = torch.cuda.get_device_properties(dev)
@@ -422,7 +423,7 @@ def run_ours(args, world, rank, local):
             "q": torch.empty_like(q), "pt": torch.empty_like(pt), "out": torch.empty_like(out),
             "lse": torch.empty_like(lse), "out_h": torch.empty(out.shape, dtype=out.dtype).pin_memory(),
             "lse_h": torch.empty(lse.shape, dtype=lse.dtype).pin_memory(), "ev": torch.cuda.Event(),
-            "plan": None})
+            "plan": None, "ws": torch.empty(plan.info()["workspace_bytes"], dtype=torch.uint8, device=dev)})
     e2e_steps = max(3, min(args.steps, 200))
 
     def e2e_step(k):
@@ -431,7 +432,7 @@ def run_ours(args, world, rank, local):
             sl["ev"].synchronize()   # step k-2's result is on the host; its buffers are free
         sl["q"].copy_(q_h, non_blocking=True)
         sl["pt"].copy_(pt_h, non_blocking=True)
-        sl["plan"] = plan_of(batch, sl["pt"])
+        sl["plan"] = plan_of(batch, sl["pt"], sl["ws"])   # the slot's workspace: its last step is done
         sl["plan"].decode(sl["q"], kv, sinks, sl["out"], sl["lse"])
         sl["out_h"].copy_(sl["out"], non_blocking=True)
         sl["lse_h"].copy_(sl["lse"], non_blocking=True)

@@ -109,9 +109,15 @@ def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream_ptr(stream=None):
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return ctypes.c_void_p(s.cuda_stream)
+    if stream is not None:
+        return ctypes.c_void_p(stream.cuda_stream)
+    if _raw_stream is not None:   # the current stream's handle without building a Stream object
+        return ctypes.c_void_p(_raw_stream(torch.cuda.current_device()))
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
 class Plan:
@@ -120,12 +126,17 @@ class Plan:
 
     qo_indptr, kv_indptr, last_page_len: host int arrays (or CPU tensors).
     page_table: int32 CUDA tensor; kept referenced by the plan.
+    workspace: optional uint8 CUDA tensor to bind instead of allocating one
+    (used when it holds at least the plan's workspace_bytes and starts on a
+    256-byte boundary); a serving loop can reuse one per step in flight, as
+    long as no launch of an older plan bound to it is still running.
     """
 
     def __init__(self, qo_indptr, kv_indptr, page_table: torch.Tensor, last_page_len,
                  num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
                  causal: bool = True, sm_scale: Optional[float] = None,
-                 num_pages: Optional[int] = None, num_sms: int = 0, stream=None):
+                 num_pages: Optional[int] = None, num_sms: int = 0, stream=None,
+                 workspace: Optional[torch.Tensor] = None):
         lib = load_library()
         self._handle = None
         qo = _i32_host(qo_indptr)
@@ -151,8 +162,12 @@ class Plan:
             num_kv_heads, head_dim, page_size, int(self.causal), self.sm_scale, int(num_pages),
             int(num_sms), ctypes.byref(handle), ctypes.byref(ws_bytes)))
         self._handle = handle
-        self.workspace = torch.empty(max(int(ws_bytes.value), 256), dtype=torch.uint8,
-                                     device=page_table.device)
+        need = max(int(ws_bytes.value), 256)
+        if (workspace is not None and workspace.is_cuda and workspace.dtype == torch.uint8
+                and workspace.numel() >= need and workspace.data_ptr() % 256 == 0):
+            self.workspace = workspace
+        else:
+            self.workspace = torch.empty(need, dtype=torch.uint8, device=page_table.device)
         _check("attn_plan_bind_workspace", lib.attn_plan_bind_workspace(
             self._handle, _ptr(self.workspace), self.workspace.numel(), _stream_ptr(stream)))
 

@@ -7,6 +7,7 @@
 // decode performance"), so decode sequences are cut into chunks of similar
 // size until the CTAs fill the GPU, and both lists are ordered longest first.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <new>
@@ -20,6 +21,29 @@ namespace {
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 bool supported_head_dim(int d) { return d == 64 || d == 128; }
+
+// SM count of the current device, queried once per device.
+bool current_sm_count(int32_t* out) {
+    constexpr int kMaxDevices = 64;
+    static std::atomic<int32_t> cache[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (dev >= 0 && dev < kMaxDevices && cache[dev].load(std::memory_order_relaxed) > 0) {
+        *out = cache[dev].load(std::memory_order_relaxed);
+        return true;
+    }
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+        cudaGetLastError();
+        return false;
+    }
+    if (dev >= 0 && dev < kMaxDevices) cache[dev].store(sms, std::memory_order_relaxed);
+    *out = sms;
+    return true;
+}
 bool supported_page_size(int p) { return p == 16 || p == 32 || p == 64 || p == 128; }
 
 }  // namespace
@@ -72,14 +96,7 @@ attn_status make_plan(bool ragged, const int32_t* qo_indptr, const int32_t* kv_i
     const int64_t total_rows = batch > 0 ? qo_indptr[batch] : 0;
     if (total_rows * num_qo_heads > (int64_t)INT32_MAX) return ATTN_ERR_UNSUPPORTED;
 
-    if (num_sms == 0) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-            cudaGetLastError();
-            return ATTN_ERR_CUDA;
-        }
-    }
+    if (num_sms == 0 && !current_sm_count(&num_sms)) return ATTN_ERR_CUDA;
 
     attn_plan_s* plan = new (std::nothrow) attn_plan_s();
     if (!plan) return ATTN_ERR_INVALID_ARG;
@@ -347,14 +364,7 @@ extern "C" attn_status attn_graph_plan(int32_t max_batch, int32_t num_qo_heads, 
     if (!supported_head_dim(head_dim) || !supported_page_size(page_size)) return ATTN_ERR_UNSUPPORTED;
     if ((int64_t)max_batch * num_qo_heads > (int64_t)INT32_MAX) return ATTN_ERR_UNSUPPORTED;
     if (max_batch > kGraphMaxBatch) return ATTN_ERR_UNSUPPORTED;   // the device planner's shared memory
-    if (num_sms == 0) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-            cudaGetLastError();
-            return ATTN_ERR_CUDA;
-        }
-    }
+    if (num_sms == 0 && !current_sm_count(&num_sms)) return ATTN_ERR_CUDA;
     // Capacity of the device-built work list.  With the host planner's rule
     // (chunk >= total blocks / target, at most 512 blocks, each request at
     // least one chunk per head slice) the units never exceed
