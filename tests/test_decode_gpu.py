@@ -161,3 +161,38 @@ def test_bad_page_id_is_flagged_not_faulted():
     plan.decode(q, kv, sk, out, None)
     assert plan.device_error() & 1
     assert plan.device_error() == 0     # cleared by the read
+
+
+def test_caller_workspace_reused_across_plans():
+    """A caller-provided workspace, bound to a new plan per step (as a serving
+    loop does once the previous step is done), gives the same bits as a plan
+    with its own workspace; a too-small or misaligned one is not used."""
+    from paged_kv_attention_sink_gb300 import binding
+    b1, b2 = syn.gptoss_decode(seed=3, batch=24), syn.tiny_decode(1)
+    ws = torch.empty(64 << 20, dtype=torch.uint8, device="cuda")
+    for batch in (b1, b2, b1):
+        q, kv, pt, sk = to_device(batch)
+        own = make_plan(batch, pt)
+        shared = binding.Plan(batch.qo_indptr, batch.kv_indptr, pt, batch.last_page_len, batch.num_qo_heads,
+                              batch.num_kv_heads, batch.head_dim, batch.page_size, causal=batch.causal,
+                              sm_scale=batch.sm_scale, num_pages=batch.num_pages, workspace=ws)
+        assert shared.workspace.data_ptr() == ws.data_ptr()
+        o1, o2 = torch.empty_like(q), torch.empty_like(q)
+        l1 = torch.empty(batch.total_rows, batch.num_qo_heads, device="cuda")
+        l2 = torch.empty_like(l1)
+        own.decode(q, kv, sk, o1, l1)
+        shared.decode(q, kv, sk, o2, l2)
+        torch.cuda.synchronize()
+        assert own.device_error() == 0 and shared.device_error() == 0
+        assert torch.equal(o1.view(torch.int16), o2.view(torch.int16)) and torch.equal(l1, l2)
+        del shared
+    q, kv, pt, sk = to_device(b1)
+    small = torch.empty(256, dtype=torch.uint8, device="cuda")
+    p = binding.Plan(b1.qo_indptr, b1.kv_indptr, pt, b1.last_page_len, b1.num_qo_heads, b1.num_kv_heads,
+                     b1.head_dim, b1.page_size, causal=b1.causal, sm_scale=b1.sm_scale, num_pages=b1.num_pages,
+                     workspace=small)
+    assert p.workspace.data_ptr() != small.data_ptr()
+    p2 = binding.Plan(b1.qo_indptr, b1.kv_indptr, pt, b1.last_page_len, b1.num_qo_heads, b1.num_kv_heads,
+                      b1.head_dim, b1.page_size, causal=b1.causal, sm_scale=b1.sm_scale, num_pages=b1.num_pages,
+                      workspace=ws[16:])
+    assert p2.workspace.data_ptr() != ws.data_ptr() + 16
