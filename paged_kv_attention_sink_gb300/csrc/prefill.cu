@@ -28,10 +28,13 @@
 //    the row max is taken on an item's first tile only; later tiles keep it
 //    unless their P row sum passes 2^64 (then the max is raised, O rescaled in
 //    TMEM and the tile recomputed); P is rounded to bf16 and O is normalised
-//    by the row sum of that rounded P, while lse uses the unrounded sum.
+//    by the row sum of that rounded P, while lse uses the unrounded sum.  At
+//    D = 64 a full 128-row tile's O leaves through the head slot's P buffer
+//    in shared memory and one TMA store; ragged last tiles use plain stores.
 //
-// TMEM (512 columns): S0 S1 (128 each), O0 O1 (D each), and at D = 64 P0 P1
-// (64 each); at D = 128 P aliases the first half of S.
+// TMEM (512 columns): S0 S1 (128 each), O0 O1 (D each, plus at D = 64 the
+// 16 row-sum columns), and at D = 64 P0 P1 (keys 0..63, 32 columns each); at
+// D = 128 P aliases the first half of S.
 // Every wait is bounded; a timeout sets the device error word.
 #include <cuda.h>
 
