@@ -106,7 +106,9 @@ def _i32_host(a) -> np.ndarray:
 
 
 def _ptr(t: Optional[torch.Tensor]):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # A plain int: ctypes converts it for the c_void_p parameter (cheaper than
+    # building a c_void_p object on every call).
+    return None if t is None else t.data_ptr()
 
 
 _raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
@@ -114,10 +116,10 @@ _raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 def _stream_ptr(stream=None):
     if stream is not None:
-        return ctypes.c_void_p(stream.cuda_stream)
+        return stream.cuda_stream
     if _raw_stream is not None:   # the current stream's handle without building a Stream object
-        return ctypes.c_void_p(_raw_stream(torch.cuda.current_device()))
-    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        return _raw_stream(torch.cuda.current_device())
+    return torch.cuda.current_stream().cuda_stream
 
 
 class Plan:
@@ -157,8 +159,7 @@ class Plan:
         handle = ctypes.c_void_p()
         ws_bytes = ctypes.c_size_t()
         _check("attn_plan", lib.attn_plan(
-            qo.ctypes.data_as(ctypes.c_void_p), kv.ctypes.data_as(ctypes.c_void_p),
-            _ptr(page_table), lpl.ctypes.data_as(ctypes.c_void_p), self.batch, num_qo_heads,
+            qo.ctypes.data, kv.ctypes.data, _ptr(page_table), lpl.ctypes.data, self.batch, num_qo_heads,
             num_kv_heads, head_dim, page_size, int(self.causal), self.sm_scale, int(num_pages),
             int(num_sms), ctypes.byref(handle), ctypes.byref(ws_bytes)))
         self._handle = handle
