@@ -213,7 +213,7 @@ ATTN_API attn_status attn_merge_states(const void* va, const float* lsea, const 
  * memory when they run attention (for example an engine that replays a
  * captured CUDA graph, or one that reserves its memory budget up front and
  * forbids cudaMalloc, and with it cudaMalloc's implicit device sync, while it
- * serves).  The paper has no counterpart: this is an interface addition.
+ * serves).  No source describes such a call: this is an interface addition.
  *
  * Same arguments and results as attn_decode, but the plan needs no bound
  * workspace: the work list, split-KV partial states, merge counters and error
