@@ -143,11 +143,11 @@ def tiny_decode(seed: int = 0) -> Batch:
     return make_batch("tiny_decode", [1, 1], [256, 97], 8, 2, 64, 16, pool_pages=64, rng=rng)
 
 
-def gptoss_decode(seed: int = 0, batch: int = 64) -> Batch:
+def gptoss_decode(seed: int = 0, batch: int = 64, fill_pool: bool = True) -> Batch:
     """gpt-oss-120b-shaped decode: kv_len ~ U[1024, 8192], Hq 64 / Hkv 8, D 64, P 16."""
     rng = _rng(seed)
     kv = rng.integers(1024, 8192, size=batch, endpoint=True)
-    return make_batch("gptoss_decode", [1] * batch, kv, 64, 8, 64, 16, rng=rng)
+    return make_batch("gptoss_decode", [1] * batch, kv, 64, 8, 64, 16, rng=rng, fill_pool=fill_pool)
 
 
 def gptoss_prefill(seed: int = 0, n_seq: int = 8) -> Batch:
