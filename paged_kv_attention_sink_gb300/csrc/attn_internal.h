@@ -1,9 +1,12 @@
 // Internal declarations shared by the planner (host) and the kernels.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <vector>
+
+#include <cuda_runtime.h>
 
 #include "../../include/attn.h"
 
@@ -63,6 +66,30 @@ struct WorkspaceLayout {
 // CTAs of the decode kernel resident per SM for a head dim (matches its
 // shared-memory footprint); defined next to the kernel.
 int decode_ctas_per_sm(int head_dim);
+
+// SM count of the current device, queried once per device (thread-safe).
+bool current_sm_count(int32_t* out);
+
+// Device ordinals that the per-device caches below cover; a higher ordinal
+// is served without a cache.
+constexpr int kMaxDevices = 64;
+
+// Runs `setup` (returning cudaError_t) until it first succeeds on the current
+// device, then only checks a flag.  Kernel attributes such as the dynamic
+// shared-memory limit belong to one device's context, so a process that
+// drives several devices sets them on each.  Two threads may both run setup
+// the first time; it must be idempotent.
+template <class F>
+cudaError_t once_per_device(std::atomic<bool> (&done)[kMaxDevices], F&& setup) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const bool cached = dev >= 0 && dev < kMaxDevices;
+    if (cached && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    e = setup();
+    if (e == cudaSuccess && cached) done[dev].store(true, std::memory_order_release);
+    return e;
+}
 
 }  // namespace attn
 

@@ -675,12 +675,11 @@ template <int D, bool kTwoRows, bool kPersistent>
 cudaError_t launch(const CUtensorMap& map, const DecodeArgs& args, int grid, cudaStream_t stream) {
     using C = DecodeCfg<D>;
     auto kernel = decode_sink_attn_kernel<D, kTwoRows, kPersistent>;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static std::atomic<bool> configured[kMaxDevices];
+    cudaError_t e = once_per_device(configured, [&] {
+        return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    });
+    if (e != cudaSuccess) return e;
     kernel<<<grid, C::kWarps * 32, C::kSmem, stream>>>(map, args);
     return cudaGetLastError();
 }

@@ -84,14 +84,11 @@ head_slice_kernel(uint4* __restrict__ pool, uint4* __restrict__ buf, const int32
     }
 }
 
+// Grid of a grid-stride copy: one CTA per work item up to `per_sm` CTAs per
+// SM; 0 when the SM count cannot be queried.
 int copy_grid(int64_t work_items, int per_sm) {
-    static int sms = 0;
-    if (sms == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
-            sms = 132;
-    }
+    int32_t sms = 0;
+    if (!current_sm_count(&sms)) return 0;
     const int64_t cap = (int64_t)sms * per_sm;
     return (int)(work_items < cap ? (work_items > 0 ? work_items : 1) : cap);
 }
@@ -104,6 +101,7 @@ attn_status launch_append_kv(attn_plan_s* plan, const void* k_new, const void* v
     if (rows == 0) return ATTN_OK;
     const int32_t chunks = plan->D / 8;
     const int grid = copy_grid((rows + kCopyThreads / 32 - 1) / (kCopyThreads / 32), 8);
+    if (grid == 0) return ATTN_ERR_CUDA;
     append_kv_kernel<<<grid, kCopyThreads, 0, stream>>>(
         static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), static_cast<uint4*>(kv_cache),
         reinterpret_cast<const int2*>(plan->ws + plan->layout.append), plan->page_table, rows, plan->Hkv,
@@ -117,6 +115,7 @@ attn_status launch_head_slice(bool unpack, void* kv_cache, void* buf, const int3
     if (n == 0) return ATTN_OK;
     const int32_t head_chunks = P * D / 8;
     const int grid = copy_grid(n * 2, 4);
+    if (grid == 0) return ATTN_ERR_CUDA;
     if (unpack)
         head_slice_kernel<true><<<grid, kCopyThreads, 0, stream>>>(
             static_cast<uint4*>(kv_cache), static_cast<uint4*>(buf), page_ids, n, Hkv, head_chunks, h0, nh,

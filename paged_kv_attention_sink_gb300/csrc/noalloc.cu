@@ -23,7 +23,7 @@
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = 16u << 20;   // 16 MiB per device
-constexpr int kMaxDevices = 64;
+using attn::kMaxDevices;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 

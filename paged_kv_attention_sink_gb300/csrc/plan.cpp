@@ -21,10 +21,13 @@ namespace {
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 bool supported_head_dim(int d) { return d == 64 || d == 128; }
+bool supported_page_size(int p) { return p == 16 || p == 32 || p == 64 || p == 128; }
 
-// SM count of the current device, queried once per device.
+}  // namespace
+
+namespace attn {
+
 bool current_sm_count(int32_t* out) {
-    constexpr int kMaxDevices = 64;
     static std::atomic<int32_t> cache[kMaxDevices] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -44,9 +47,8 @@ bool current_sm_count(int32_t* out) {
     *out = sms;
     return true;
 }
-bool supported_page_size(int p) { return p == 16 || p == 32 || p == 64 || p == 128; }
 
-}  // namespace
+}  // namespace attn
 
 namespace {
 

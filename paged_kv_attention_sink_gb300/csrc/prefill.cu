@@ -756,17 +756,16 @@ cudaError_t launch(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorM
                    const PrefillArgs& args, int grid, cudaStream_t stream) {
     using C = PrefillCfg<D>;
     auto kernel = prefill_sink_attn_kernel<D, kRagged>;
-    static bool configured = false;
-    if (!configured) {
+    static std::atomic<bool> configured[kMaxDevices];
+    cudaError_t e = once_per_device(configured, [&] {
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
-        if (e != cudaSuccess) return e;
+        cudaError_t err = cudaFuncGetAttributes(&fa, kernel);
+        if (err != cudaSuccess) return err;
         // The register split above assumes this launch size; refuse otherwise.
         if (fa.numRegs < C::kRegsLaunch) return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+        return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    });
+    if (e != cudaSuccess) return e;
     kernel<<<grid, C::kThreads, C::kSmem, stream>>>(qm, km, vm, om, args);
     return cudaGetLastError();
 }

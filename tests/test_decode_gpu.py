@@ -196,3 +196,18 @@ def test_caller_workspace_reused_across_plans():
                       b1.head_dim, b1.page_size, causal=b1.causal, sm_scale=b1.sm_scale, num_pages=b1.num_pages,
                       workspace=ws[16:])
     assert p2.workspace.data_ptr() != ws.data_ptr() + 16
+
+
+def test_decode_many_short_requests():
+    """1024 decode requests of 1..200 tokens: many more work units than CTA
+    slots, most of them unsplit, several shorter than one 16-token block."""
+    rng = np.random.default_rng(21)
+    kv = rng.integers(1, 201, size=1024).tolist()
+    batch = syn.make_batch("many", [1] * 1024, kv, 64, 8, 64, 16, seed=21)
+    out, lse, _ = run_decode(batch)
+    rows, heads = sample_pairs(batch, decode_rows(batch), 1024, seed=4)
+    ref_out, ref_lse = oracle.sink_attention(batch, rows=rows, heads=heads)
+    ri = torch.from_numpy(rows).cuda()
+    hi = torch.from_numpy(heads).long().cuda()
+    check_close(out[ri, hi], lse[ri, hi], ref_out, ref_lse, "1024 short decodes")
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()

@@ -162,3 +162,18 @@ def test_graph_batch_beyond_capacity_sets_plan_error():
     plan = _graph_plan(buf, 2, b)
     _decode(plan, buf)
     assert plan.device_error() == 4
+
+
+def test_graph_decode_at_planner_capacity():
+    """4096 requests, the most one device-planned replay can order."""
+    rng = np.random.default_rng(22)
+    kv = rng.integers(1, 300, size=4096).tolist()
+    b = syn.make_batch("cap4096", [1] * 4096, kv, 16, 2, 64, 16, seed=22)
+    buf = Buffers(4096, 16, 2, 64, 16, b.num_pages, len(b.page_table))
+    buf.load(b)
+    plan = _graph_plan(buf, 4096, b)
+    _decode(plan, buf)
+    torch.cuda.synchronize()
+    assert plan.device_error() == 0
+    _check(b, buf, n=1024, seed=5, what="graph decode, 4096 requests")
+    assert torch.isfinite(buf.out.float()).all()

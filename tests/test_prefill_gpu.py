@@ -172,3 +172,21 @@ def test_prefill_persistent_item_streams(num_sms):
     torch.cuda.synchronize()
     assert plan.device_error() == 0
     _check_rows(batch, out, lse, what=f"sms={num_sms}")
+
+
+def test_prefill_long_sequence_sampled():
+    """A 32K-token sequence whose last 8K tokens are the prefill rows (24K cached
+    prefix), Qwen3-like D = 128 and P = 64: 256 KV tiles per item, so the
+    running max is reused across many tiles and the item lists are long.  The
+    first and last rows of the long request are always checked."""
+    batch = syn.make_batch("long", [8192, 300], [32768, 300], 16, 4, 128, 64, seed=13)
+    out, lse, _ = run_prefill(batch)
+    rows, heads = sample_pairs(batch, prefill_rows(batch), 384, seed=3)
+    edge = np.array([0, 0, 8191, 8191, 8192, 8491], dtype=np.int64)
+    rows = np.concatenate([rows, edge])
+    heads = np.concatenate([heads, np.array([0, 15, 3, 12, 7, 8], dtype=np.int32)])
+    ref_out, ref_lse = oracle.sink_attention(batch, rows=rows, heads=heads)
+    ri = torch.from_numpy(rows).cuda()
+    hi = torch.from_numpy(heads).long().cuda()
+    check_close(out[ri, hi], lse[ri, hi], ref_out, ref_lse, "long prefill")
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
