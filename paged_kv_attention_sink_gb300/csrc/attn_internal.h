@@ -103,6 +103,7 @@ struct attn_plan_s {
     bool graph = false;                   // attn_graph_plan: decode work list built on the device
                                           // (batch = max batch; n_partials / n_groups = capacities)
     int64_t kv_tokens = 0;                // ragged: rows of K and V (kv_indptr[batch])
+    int64_t graph_kv_blocks = 0;          // graph: 16-token blocks a batch may hold in total
 
     std::vector<attn::DecodeUnit> units;
     std::vector<attn::PrefillItem> items;

@@ -463,6 +463,7 @@ struct GraphPlanArgs {
     const int32_t* batch;           // device scalar
     int32_t max_batch, Hq, Hkv, P, n_slices;
     int64_t target_units;
+    int64_t cap_blocks;             // 16-token blocks the plan's capacity allows
     int32_t cap_units, cap_groups;
     DecodeUnit* units;
     int32_t* n_units;
@@ -500,10 +501,15 @@ __device__ void block_scan3(int (&v)[3], int (&total)[3], int* sh /* [3][32] */)
     __syncthreads();
 }
 
-// Dynamic shared memory of the planner: 7 int32 per request slot (page
-// base, kv_len, sorted order, chunk count, and the exclusive offsets of units,
-// partial slots and groups).
+// Dynamic shared memory of the planner: 7 int32 per request slot (page base
+// and kv_len by request; request, chunk count and the exclusive offsets of
+// units, partial slots and groups by sorted position).
 inline size_t plan_smem_bytes(int max_batch) { return (size_t)max_batch * 7 * sizeof(int); }
+
+// Requests one planner thread owns (request tid + k * kPlanThreads); their
+// lengths, chunk counts and unit lengths stay in registers.
+constexpr int kPlanPerThread = (kGraphMaxBatch + kPlanThreads - 1) / kPlanThreads;
+static_assert(kPlanPerThread * kPlanThreads >= kGraphMaxBatch, "planner request ownership");
 
 // Token range [c * nblk / nc, (c + 1) * nblk / nc) blocks, in 32-bit
 // arithmetic when the product fits (the common case).
@@ -534,46 +540,66 @@ __global__ void __launch_bounds__(kPlanThreads) decode_graph_plan_kernel(const G
     }
     for (int k = tid; k < kLenBuckets; k += kPlanThreads) s_hist[k] = 0;
 
-    // Pass 1: kv lengths, and all 16-token blocks -> chunk size (two waves of CTAs).
+    // Pass 1: kv lengths of the owned requests, and all 16-token blocks ->
+    // chunk size (two waves of CTAs).  kv_len fits 32 bits (checked), so
+    // block counts (< 2^27) do too.
+    int kv[kPlanPerThread], nc[kPlanPerThread], ulen[kPlanPerThread];
     long long blocks = 0;
-    for (int b = tid; b < B; b += kPlanThreads) {
+#pragma unroll
+    for (int k = 0; k < kPlanPerThread; ++k) {
+        const int b = tid + k * kPlanThreads;
+        kv[k] = -1;
+        if (b >= B) continue;
         const int32_t base = p.kv_indptr[b];
         const int64_t np = (int64_t)p.kv_indptr[b + 1] - base;
         const int32_t lpl = p.last_page_len[b];
-        int64_t kv = -1;
-        if (np >= 1 && lpl >= 1 && lpl <= p.P) kv = (np - 1) * p.P + lpl;
-        if (kv < 0 || kv > INT32_MAX) {
+        int64_t len = -1;
+        if (np >= 1 && lpl >= 1 && lpl <= p.P) len = (np - 1) * p.P + lpl;
+        if (len < 0 || len > INT32_MAX) {
             atomicOr(p.err, ATTN_DEVICE_ERR_PLAN);
-            kv = -1;
+            len = -1;
         }
+        kv[k] = (int)len;
         s_base[b] = base;
-        s_kv[b] = (int)kv;
-        if (kv > 0) blocks += (kv + kBlockTokens - 1) / kBlockTokens;
+        s_kv[b] = kv[k];
+        if (len > 0) blocks += (len + kBlockTokens - 1) / kBlockTokens;
     }
     for (int o = 16; o > 0; o >>= 1) blocks += __shfl_xor_sync(0xffffffffu, blocks, o);
     if (lane == 0) s_blocks[warp] = blocks;
     __syncthreads();
     long long total_blocks = 0;
     for (int w = 0; w < kPlanThreads / 32; ++w) total_blocks += s_blocks[w];
+    if (total_blocks > p.cap_blocks) {
+        // More KV than the plan was sized for: the unit bound below (and the
+        // 32-bit counts that rely on it) would not hold.  Same value in every
+        // thread, so the whole block leaves here.
+        if (tid == 0) {
+            atomicOr(p.err, ATTN_DEVICE_ERR_PLAN);
+            *p.n_units = 0;
+            p.queue[0] = p.queue[1] = 0;
+        }
+        return;
+    }
     total_blocks *= (long long)p.Hkv * p.n_slices;
-    int64_t chunk = (int64_t)((total_blocks + p.target_units - 1) / p.target_units);
-    chunk = min((int64_t)kDecodeMaxChunkBlocks, max((int64_t)kDecodeMinChunkBlocks, chunk));
-    auto n_chunks_of = [&](int64_t kv) -> int {
-        if (kv < 0) return 0;
-        const int64_t nblk = (kv + kBlockTokens - 1) / kBlockTokens;
-        int64_t n = max((int64_t)1, (nblk + chunk / 2) / chunk);
-        n = max(n, (int64_t)((nblk + kDecodeMaxChunkBlocks - 1) / kDecodeMaxChunkBlocks));
-        return (int)n;
-    };
-    auto unit_len = [&](int64_t kv, int nc) -> int {   // blocks in the request's longest chunk
-        return nc > 0 ? (int)(((kv + kBlockTokens - 1) / kBlockTokens + nc - 1) / nc) : 0;
-    };
+    const uint32_t chunk = (uint32_t)min((long long)kDecodeMaxChunkBlocks,
+                                         max((long long)kDecodeMinChunkBlocks,
+                                             (total_blocks + p.target_units - 1) / p.target_units));
 
-    // Pass 2: order the requests by unit length, longest first (counting sort
-    // over the 513 possible lengths), as the host planner orders its units.
-    for (int b = tid; b < B; b += kPlanThreads) {
-        const int64_t kv = s_kv[b];
-        atomicAdd(&s_hist[kDecodeMaxChunkBlocks - unit_len(kv, n_chunks_of(kv))], 1);
+    // Pass 2: order the requests by unit length (blocks in the request's
+    // longest chunk), longest first, as the host planner orders its units: a
+    // counting sort over the 513 possible lengths.
+#pragma unroll
+    for (int k = 0; k < kPlanPerThread; ++k) {
+        nc[k] = 0;
+        ulen[k] = 0;
+        if (kv[k] >= 0) {
+            const uint32_t nblk = ((uint32_t)kv[k] + kBlockTokens - 1) / kBlockTokens;
+            const uint32_t n = max(max(1u, (nblk + chunk / 2) / chunk),
+                                   (nblk + kDecodeMaxChunkBlocks - 1) / kDecodeMaxChunkBlocks);
+            nc[k] = (int)n;
+            ulen[k] = (int)((nblk + n - 1) / n);
+        }
+        if (tid + k * kPlanThreads < B) atomicAdd(&s_hist[kDecodeMaxChunkBlocks - ulen[k]], 1);
     }
     __syncthreads();
     if (warp == 0) {   // exclusive scan of the histogram, 17 buckets per lane
@@ -599,9 +625,13 @@ __global__ void __launch_bounds__(kPlanThreads) decode_graph_plan_kernel(const G
         }
     }
     __syncthreads();
-    for (int b = tid; b < B; b += kPlanThreads) {
-        const int64_t kv = s_kv[b];
-        s_order[atomicAdd(&s_hist[kDecodeMaxChunkBlocks - unit_len(kv, n_chunks_of(kv))], 1)] = b;
+#pragma unroll
+    for (int k = 0; k < kPlanPerThread; ++k) {
+        const int b = tid + k * kPlanThreads;
+        if (b >= B) continue;
+        const int pos = atomicAdd(&s_hist[kDecodeMaxChunkBlocks - ulen[k]], 1);
+        s_order[pos] = b;
+        s_nc[pos] = nc[k];
     }
     __syncthreads();
 
@@ -612,8 +642,7 @@ __global__ void __launch_bounds__(kPlanThreads) decode_graph_plan_kernel(const G
     const int i0 = min(B, tid * per), i1 = min(B, i0 + per);
     int v[3] = {0, 0, 0}, tot[3];
     for (int i = i0; i < i1; ++i) {
-        const int nc = n_chunks_of(s_kv[s_order[i]]);
-        s_nc[i] = nc;
+        const int nc = s_nc[i];
         v[0] += nc * per_req;
         if (nc > 1) {
             v[1] += nc * per_req;
@@ -759,21 +788,22 @@ attn_status launch_decode_graph(attn_plan_s* plan, const int32_t* kv_indptr, con
     gp.P = plan->P;
     gp.n_slices = (plan->Hq / plan->Hkv + kMaxSliceHeads - 1) / kMaxSliceHeads;
     gp.target_units = 2LL * plan->num_sms * decode_ctas_per_sm(plan->D);
+    gp.cap_blocks = plan->graph_kv_blocks;
     gp.cap_units = plan->n_partials;   // graph plans size units and partial slots alike
     gp.cap_groups = plan->n_groups;
     gp.units = reinterpret_cast<DecodeUnit*>(plan->ws + plan->layout.units);
     gp.n_units = reinterpret_cast<int32_t*>(plan->ws + plan->layout.n_units);
     gp.queue = reinterpret_cast<int32_t*>(plan->ws + plan->layout.counters);
     gp.err = reinterpret_cast<int32_t*>(plan->ws + plan->layout.err);
-    const size_t smem = plan_smem_bytes(plan->batch);
-    static size_t configured = 0;
-    if (smem > 48 * 1024 && smem > configured) {
-        if (cudaFuncSetAttribute(decode_graph_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess)
-            return ATTN_ERR_CUDA;
-        configured = smem;
-    }
-    decode_graph_plan_kernel<<<1, kPlanThreads, smem, stream>>>(gp);
+    // The shared-memory limit is raised once per device to what the largest
+    // graph plan needs; each launch asks only for its own plan's share.
+    static std::atomic<bool> configured[kMaxDevices];
+    if (once_per_device(configured, [] {
+            return cudaFuncSetAttribute(decode_graph_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)plan_smem_bytes(kGraphMaxBatch));
+        }) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    decode_graph_plan_kernel<<<1, kPlanThreads, plan_smem_bytes(plan->batch), stream>>>(gp);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     DecodeArgs a = make_args(plan, plan->ws, q, sinks, out, lse);
     a.queue = gp.queue;

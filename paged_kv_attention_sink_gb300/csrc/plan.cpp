@@ -396,6 +396,7 @@ extern "C" attn_status attn_graph_plan(int32_t max_batch, int32_t num_qo_heads, 
     plan->page_table = page_table;
     plan->n_partials = (int32_t)cap_units;
     plan->n_groups = (int32_t)cap_groups;
+    plan->graph_kv_blocks = kv_blocks;
 
     WorkspaceLayout& L = plan->layout;
     size_t off = 0;

@@ -177,3 +177,17 @@ def test_graph_decode_at_planner_capacity():
     assert plan.device_error() == 0
     _check(b, buf, n=1024, seed=5, what="graph decode, 4096 requests")
     assert torch.isfinite(buf.out.float()).all()
+
+
+def test_graph_kv_beyond_plan_capacity_sets_plan_error():
+    """A batch holding more KV than the plan was sized for is refused on the
+    device (no units, error word set) instead of overrunning the work list."""
+    b = syn.make_batch("kvcap", [1, 1], [40, 90], 8, 2, 64, 16, seed=14)
+    buf = Buffers(2, 8, 2, 64, 16, b.num_pages, len(b.page_table))
+    buf.load(b)
+    plan = _graph_plan(buf, 2, b, max_kv_tokens=64)   # 9 blocks needed, 64 / 16 + 2 = 6 allowed
+    _decode(plan, buf)
+    torch.cuda.synchronize()
+    assert plan.device_error() == 4
+    assert len(plan.device_units()) == 0
+    assert torch.isnan(buf.out.float()).all()
