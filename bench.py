@@ -13,6 +13,8 @@ timed kernel starts with a cold L2 that holds no dirty lines (otherwise the
 write-back of the memset's ~129 MB of dirty lines lands inside the timed
 kernel and is charged to it).  The prefill leg (gpt-oss-120b-shaped ragged causal
 prefill) is reported in TFLOP/s of visible (query, key) pairs x 4 * head_dim.
+`value` and `ms_per_step` use the total of the K timed steps (the mean);
+`ms_per_step_median` gives the median step beside it.
 
 One step = one pass of the hot path over one batch: the plan is built once
 per batch (host), then attn_decode runs (and attn_prefill for the prefill
@@ -638,7 +640,8 @@ def run_ours(args, world, rank, local):
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "ms_per_step": total_ms / args.steps, "ms_per_step_median": statistics.median(times),
+            "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": "gptoss_decode", "batch": batch.batch_size,
                        "kv_len": "U[1024,8192]", "Hq": 64, "Hkv": 8, "head_dim": 64,
