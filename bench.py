@@ -21,7 +21,8 @@ per batch (host), then attn_decode runs (and attn_prefill for the prefill
 leg).  `e2e` times the same decode through the public API from pinned host
 buffers: H2D of q and the page table, planning and work-list upload, the
 launch, and D2H of out and lse, every step, with two steps in flight (the
-host plans step k while the GPU runs step k-1).
+host plans step k while the GPU runs step k-1) and the copies on their own
+streams (they overlap the neighbouring steps' decodes).
 
 Multi-GPU: the path shards by request with no exchange, so N ranks run N
 independent replicas ("scaling": "weak"); value = all ranks' bytes / max
@@ -416,29 +417,48 @@ def run_ours(args, world, rank, local):
     # in flight, as a serving loop would run them: the host plans and launches
     # step k (H2D of its q and page table, attn_plan + workspace upload,
     # attn_decode, D2H of its out and lse) while the GPU still runs step k-1,
-    # and waits for a step's read-back before reusing its buffers.
-    q_h = torch.from_numpy(batch.q.view(np.int16)).view(torch.bfloat16).pin_memory()
-    pt_h = torch.from_numpy(batch.page_table).pin_memory()
+    # and waits for a step's read-back before reusing its buffers.  The
+    # uploads run on one copy stream and the read-backs on another, ordered
+    # against the decode on the compute stream by events, so a step's copies
+    # overlap its neighbours' decodes.
+    # q and the page table share one pinned host buffer and one device buffer
+    # per slot (one upload); out and lse likewise (one read-back).
+    q_bytes, pt_bytes = q.numel() * 2, pt.numel() * 4
+    out_bytes, lse_bytes = out.numel() * 2, lse.numel() * 4
+    in_h = torch.empty(q_bytes + pt_bytes, dtype=torch.uint8).pin_memory()
+    in_h[:q_bytes].copy_(torch.from_numpy(batch.q.view(np.uint8).reshape(-1)))
+    in_h[q_bytes:].copy_(torch.from_numpy(batch.page_table.view(np.uint8).reshape(-1)))
     e2e_slots = []
     for _ in range(2):
+        d_in = torch.empty(q_bytes + pt_bytes, dtype=torch.uint8, device=dev)
+        d_res = torch.empty(out_bytes + lse_bytes, dtype=torch.uint8, device=dev)
         e2e_slots.append({
-            "q": torch.empty_like(q), "pt": torch.empty_like(pt), "out": torch.empty_like(out),
-            "lse": torch.empty_like(lse), "out_h": torch.empty(out.shape, dtype=out.dtype).pin_memory(),
-            "lse_h": torch.empty(lse.shape, dtype=lse.dtype).pin_memory(), "ev": torch.cuda.Event(),
+            "in": d_in, "q": d_in[:q_bytes].view(torch.bfloat16).view(q.shape),
+            "pt": d_in[q_bytes:].view(torch.int32),
+            "res": d_res, "out": d_res[:out_bytes].view(torch.bfloat16).view(out.shape),
+            "lse": d_res[out_bytes:].view(torch.float32).view(lse.shape),
+            "res_h": torch.empty(out_bytes + lse_bytes, dtype=torch.uint8).pin_memory(),
+            "ev": torch.cuda.Event(), "uploaded": torch.cuda.Event(), "decoded": torch.cuda.Event(),
             "plan": None, "ws": torch.empty(plan.info()["workspace_bytes"], dtype=torch.uint8, device=dev)})
     e2e_steps = max(3, min(args.steps, 200))
+    up_stream, down_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    torch.cuda.synchronize()   # the slots' buffers exist before other streams touch them
 
     def e2e_step(k):
         sl = e2e_slots[k % 2]
         if sl["plan"] is not None:
             sl["ev"].synchronize()   # step k-2's result is on the host; its buffers are free
-        sl["q"].copy_(q_h, non_blocking=True)
-        sl["pt"].copy_(pt_h, non_blocking=True)
-        sl["plan"] = plan_of(batch, sl["pt"], sl["ws"])   # the slot's workspace: its last step is done
-        sl["plan"].decode(sl["q"], kv, sinks, sl["out"], sl["lse"])
-        sl["out_h"].copy_(sl["out"], non_blocking=True)
-        sl["lse_h"].copy_(sl["lse"], non_blocking=True)
-        sl["ev"].record()
+        with torch.cuda.stream(up_stream):
+            sl["in"].copy_(in_h, non_blocking=True)
+            sl["plan"] = plan_of(batch, sl["pt"], sl["ws"])   # binds: the work list goes up on up_stream
+            sl["uploaded"].record(up_stream)
+        stream.wait_event(sl["uploaded"])
+        sl["plan"].decode(sl["q"], kv, sinks, sl["out"], sl["lse"], stream=stream)
+        sl["decoded"].record(stream)
+        down_stream.wait_event(sl["decoded"])
+        with torch.cuda.stream(down_stream):
+            sl["res_h"].copy_(sl["res"], non_blocking=True)
+        sl["ev"].record(down_stream)
 
     for k in range(3):
         e2e_step(k)
@@ -449,14 +469,15 @@ def run_ours(args, world, rank, local):
         e2e_step(k)
     torch.cuda.synchronize()
     e2e_s = max_over_ranks(time.perf_counter() - t0, world)
-    if not torch.equal(e2e_slots[0]["out_h"].view(torch.int16), e2e_slots[1]["out_h"].view(torch.int16)):
+    if not torch.equal(e2e_slots[0]["res_h"], e2e_slots[1]["res_h"]):
         raise RuntimeError("end-to-end decode steps on the same batch disagree")
     units = plan.info()["num_decode_units"]
-    h2d = q_h.numel() * 2 + pt_h.numel() * 4 + units * 48
-    d2h = e2e_slots[0]["out_h"].numel() * 2 + e2e_slots[0]["lse_h"].numel() * 4
+    h2d = in_h.numel() + units * 48
+    d2h = e2e_slots[0]["res_h"].numel()
     e2e = {"value": world * bytes_step * e2e_steps / e2e_s / 1e9, "unit": "GB/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "ms_per_step": e2e_s * 1e3 / e2e_steps, "steps_in_flight": 2}
+           "ms_per_step": e2e_s * 1e3 / e2e_steps, "steps_in_flight": 2,
+           "streams": "uploads, decode and read-backs on three streams, ordered by events"}
 
     # ---- prefill leg (TFLOP/s), if the kernel is available
     prefill = None
