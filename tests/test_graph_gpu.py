@@ -62,11 +62,18 @@ def _check(b, buf, n=600, seed=0, what=""):
     check_close(buf.out[ri, hi], buf.lse[ri, hi], ref_out, ref_lse, what)
 
 
-def test_device_plan_equals_host_plan():
-    b = syn.gptoss_decode(0)
-    buf = Buffers(96, 64, 8, 64, 16, b.num_pages, len(b.page_table))
+@pytest.mark.parametrize("which", ["gptoss", "300_requests"])
+def test_device_plan_equals_host_plan(which):
+    """The gpt-oss batch (64 requests, capacity 96) and 300 requests of up to
+    3K tokens (capacity 600)."""
+    if which == "gptoss":
+        b, max_batch = syn.gptoss_decode(0), 96
+    else:
+        kv = np.random.default_rng(15).integers(1, 3000, size=300).tolist()
+        b, max_batch = syn.make_batch("r300", [1] * 300, kv, 64, 8, 64, 16, seed=15), 600
+    buf = Buffers(max_batch, 64, 8, 64, 16, b.num_pages, len(b.page_table))
     buf.load(b)
-    plan = _graph_plan(buf, 96, b)
+    plan = _graph_plan(buf, max_batch, b)
     _decode(plan, buf)
     dev_units = plan.device_units()
     q, kv, pt, sk = to_device(b)
