@@ -356,6 +356,19 @@ ATTN_API void attn_plan_destroy(attn_plan_t plan);
 /* Static, human-readable name of a status code. */
 ATTN_API const char* attn_status_string(attn_status status);
 
+/*
+ * attn_selftest_bounded_wait -- diagnostic of the kernels' failure detection.
+ * Launches one warp on `stream` that waits, through the same bounded mbarrier
+ * wait every kernel uses, on a barrier nothing arrives on.  The wait gives up
+ * after its wall-time limit (2 s), and the kernel writes
+ * ATTN_DEVICE_ERR_TIMEOUT to result[0] (0 had the wait completed) and the
+ * nanoseconds it waited to result[1], then returns; the context stays usable.
+ *   result   DEVICE int64 [2], caller-owned
+ * Returns ATTN_ERR_INVALID_ARG for a NULL result, ATTN_ERR_CUDA if the launch
+ * fails.
+ */
+ATTN_API attn_status attn_selftest_bounded_wait(int64_t* result, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

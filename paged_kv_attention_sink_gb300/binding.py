@@ -69,6 +69,7 @@ def _declare(lib):
         "attn_plan_device_error": (st, [p, p, p]),
         "attn_plan_destroy": (None, [p]),
         "attn_status_string": (ctypes.c_char_p, [st]),
+        "attn_selftest_bounded_wait": (st, [p, p]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -430,3 +431,17 @@ def attn_unpack_kv_heads(buf, page_ids, head_begin, kv_cache, device_error=None,
     [head_begin, head_begin + n_heads) of pages page_ids of the pool (in place)."""
     _head_slice("attn_unpack_kv_heads", kv_cache, page_ids, head_begin, buf.shape[2], buf, device_error, stream)
     return kv_cache
+
+
+def attn_selftest_bounded_wait(result=None, stream=None):
+    """Run the library's bounded-wait diagnostic (one warp waits on an mbarrier
+    nothing arrives on).  Returns the device int64 [2] result: the
+    ATTN_DEVICE_ERR_* bit the kernel recorded and the nanoseconds it waited."""
+    if result is None:
+        result = torch.full((2,), -1, dtype=torch.int64, device="cuda")
+    if not (isinstance(result, torch.Tensor) and result.is_cuda and result.dtype == torch.int64
+            and result.numel() >= 2 and result.is_contiguous()):
+        raise TypeError("result must be a contiguous int64 CUDA tensor of at least 2 elements")
+    _check("attn_selftest_bounded_wait", load_library().attn_selftest_bounded_wait(_ptr(result),
+                                                                                   _stream_ptr(stream)))
+    return result
