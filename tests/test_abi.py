@@ -243,3 +243,78 @@ def test_ragged_plan_covers_every_request(lib):
                 rows.add((r, h))
     assert rows == {(r, h) for r in range(350) for h in range(8)}
     lib.attn_plan_destroy(handle)
+
+
+def _check_decode_units(u, qo, kv, Hq, Hkv):
+    """Units cover every (decode row, query head) over [0, kv_len) in
+    contiguous chunks, chunk 0 once (it carries the sink), and the split
+    groups own disjoint partial slots."""
+    G = Hq // Hkv
+    qo_indptr = np.concatenate([[0], np.cumsum(qo)])
+    cover = {}
+    for (q_row, page_base, g, head0, nh, t0, t1, chunk, nch, group, part0, _) in u:
+        assert t0 % 16 == 0 and t0 < t1 and 1 <= nh <= 16
+        assert g * G <= head0 and head0 + nh <= (g + 1) * G
+        assert (group >= 0) == (nch > 1)
+        for hh in range(head0, head0 + nh):
+            cover.setdefault((int(q_row), hh), []).append((int(t0), int(t1), int(chunk), int(nch)))
+    decode = [b for b in range(len(qo)) if qo[b] == 1 and kv[b] > 0]
+    assert set(cover) == {(int(qo_indptr[b]), hh) for b in decode for hh in range(Hq)}
+    for b in decode:
+        for hh in range(Hq):
+            parts = sorted(cover[(int(qo_indptr[b]), hh)])
+            assert parts[0][0] == 0 and parts[-1][1] == kv[b]
+            assert all(a[1] == c[0] for a, c in zip(parts, parts[1:]))
+            assert sorted(p[2] for p in parts) == list(range(parts[0][3]))
+    slots = [int(r[10] + r[7]) for r in u if r[8] > 1]
+    assert len(slots) == len(set(slots))
+
+
+def _check_prefill_items(it, qo, kv, Hq, Hkv, causal):
+    """Items cover every (prefill row, query head) once, with the causal
+    alignment's position and visible-key bound."""
+    G = Hq // Hkv
+    qo_indptr = np.concatenate([[0], np.cumsum(qo)])
+    seen = {}
+    for (row0, nrows, page_base, kv_len, pos0, g, head0, nh, ntiles, key_end, _, _) in it:
+        b = int(np.searchsorted(qo_indptr, row0, side="right") - 1)
+        assert kv_len == kv[b] and 1 <= nrows <= 128 and nh in (1, 2)
+        assert pos0 == kv[b] - qo[b] + (row0 - qo_indptr[b])
+        end = min(kv[b], pos0 + nrows) if causal else kv[b]
+        assert key_end == end and ntiles == -(-end // 128)
+        for hh in range(head0, head0 + nh):
+            assert hh // G == g
+            for r in range(row0, row0 + nrows):
+                seen[(int(r), hh)] = seen.get((int(r), hh), 0) + 1
+    expected = {(int(r), hh) for b in range(len(qo)) if qo[b] > 1
+                for r in range(qo_indptr[b], qo_indptr[b + 1]) for hh in range(Hq)}
+    assert set(seen) == expected and all(v == 1 for v in seen.values())
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_mixed_batches_plan_correctly(lib, seed):
+    """Random mixed batches (decode, prefill on cached prefixes, empty
+    requests) over random head counts, page sizes and SM counts."""
+    rng = np.random.default_rng(500 + seed)
+    Hkv = int(rng.choice([1, 2, 4, 8]))
+    G = int(rng.choice([1, 2, 3, 8, 12, 20]))
+    Hq, P = Hkv * G, int(rng.choice([16, 32, 64, 128]))
+    B = int(rng.integers(1, 24))
+    kv = rng.integers(0, 6000, size=B)
+    kinds = rng.integers(0, 3, size=B)               # 0: decode, 1: prefill, 2: no queries
+    qo = np.where(kinds == 0, 1, np.where(kinds == 1, rng.integers(2, 400, size=B), 0))
+    qo = np.where(kv == 0, 0, np.minimum(qo, kv))      # qo_len <= kv_len; no queries on empty requests
+    pages = (kv + P - 1) // P
+    last = np.where(pages > 0, kv - (pages - 1) * P, 0)
+    causal = int(rng.integers(0, 2))
+    sms = int(rng.choice([1, 7, 152]))
+    st, h, ws = plan(lib, qo, pages, last, Hq=Hq, Hkv=Hkv, D=64, P=P, causal=causal, sms=sms)
+    assert st == OK
+    info, u, it = units_of(lib, h)
+    assert info.num_decode_requests == int(np.sum(qo == 1))
+    assert info.num_prefill_requests == int(np.sum(qo > 1))
+    assert info.total_qo_rows == int(qo.sum())
+    assert info.decode_kv_tokens == int(kv[qo == 1].sum())
+    _check_decode_units(u, qo, kv, Hq, Hkv)
+    _check_prefill_items(it, qo, kv, Hq, Hkv, causal)
+    lib.attn_plan_destroy(h)
