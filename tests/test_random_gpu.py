@@ -16,7 +16,7 @@ from helpers import check_close, make_plan, sample_pairs, syn, to_device
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("seed", range(8))
+@pytest.mark.parametrize("seed", range(24))
 def test_random_mixed_batch_matches_oracle(seed):
     rng = np.random.default_rng(900 + seed)
     Hkv = int(rng.choice([1, 2, 4, 8]))
