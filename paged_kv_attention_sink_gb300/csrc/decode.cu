@@ -453,8 +453,9 @@ decode_sink_attn_kernel(const __grid_constant__ CUtensorMap kv_map, const Decode
 // The CUDA-graph decode path plans on the device: the same split rule as the
 // host planner, from request metadata that lives in device memory, so that a
 // captured graph replays with new lengths and batch sizes (decode requests
-// only: request b is query row b).  One CTA; each thread owns a contiguous
-// range of requests.
+// only: request b is query row b).  One CTA: each thread owns requests
+// tid + k * kPlanThreads while it measures and sorts them, and a contiguous
+// range of sorted positions while it scans the unit counts.
 constexpr int kPlanThreads = 1024;
 
 struct GraphPlanArgs {
