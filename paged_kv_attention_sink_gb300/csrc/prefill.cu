@@ -18,11 +18,14 @@
 //    Tiles are 128 keys; one box per HND page, issued by its own lane (the
 //    boxes of a tile leave in one warp instruction), 128-byte swizzled.  V rows
 //    past the end of the sequence are zeroed before the MMA may read them.
-//  * warps 1 and 2, one lane each: tcgen05.mma issuers, one per head slot
-//    (neither head's MMAs queue behind the other's softmax).  S_h = Q_h K^T (both operands
-//    K-major in shared memory); O_h += P_h V with P read from tensor memory
-//    and V an MN-major shared-memory operand.  At D = 64, P has its own TMEM
-//    columns, so S_h of tile j+1 is computed while the softmax of tile j runs.
+//  * warps 1 and 2: tcgen05.mma issuers, one warp per head slot (neither
+//    head's MMAs queue behind the other's softmax), one elected lane issuing.
+//    S_h = Q_h K^T (both operands K-major in shared memory); O_h += P_h V with
+//    V an MN-major shared-memory operand.  At D = 64, P keys 0..63 come from
+//    their own TMEM columns and keys 64..127 from shared memory, and V is
+//    extended by a ones column so the same MMA accumulates the row sum of the
+//    rounded P; S_h of tile j+1 is computed while the softmax of tile j runs.
+//    At D = 128, P is read from tensor memory where S was.
 //  * warps 4-7 / 8-11: softmax of head 0 / head 1, one thread per query row
 //    (= TMEM lane).  Causal / length mask on diagonal and ragged tiles only;
 //    the row max is taken on an item's first tile only; later tiles keep it
