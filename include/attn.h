@@ -210,30 +210,46 @@ ATTN_API attn_status attn_merge_states(const void* va, const float* lsea, const 
 
 /*
  * attn_decode_noalloc -- attn_decode for callers that cannot allocate device
- * memory when they run attention (for example an engine that replays a
- * captured CUDA graph, or one that reserves its memory budget up front and
- * forbids cudaMalloc, and with it cudaMalloc's implicit device sync, while it
- * serves).  No source describes such a call: this is an interface addition.
+ * memory when they run attention: an engine that reserves its whole memory
+ * budget up front and forbids cudaMalloc while it serves (cudaMalloc may also
+ * synchronise the device and so stall every other stream).  No source
+ * describes such a call: this is an interface addition.
  *
- * Same arguments and results as attn_decode, but the plan needs no bound
- * workspace: the work list, split-KV partial states, merge counters and error
- * word live in a static 16 MiB device array inside the library, which every
- * GPU that loads the library holds until the process exits.  Plans whose
- * workspace_bytes exceed 16 MiB are rejected with ATTN_ERR_WORKSPACE_TOO_SMALL.
- * It allocates nothing (no cudaMalloc / cudaFree): each call uploads the work
- * list with cudaMemcpyAsync and zeroes the counters with cudaMemsetAsync on
- * `stream`, then launches the decode kernel.
+ * Same arguments and results as attn_decode (host-planned paged plans; a
+ * graph plan is refused with ATTN_ERR_INVALID_ARG), but the plan needs no
+ * bound workspace: the work list, split-KV partial states, merge counters and
+ * error word live in a static 16 MiB device array inside the library.  A GPU
+ * holds that array from the moment the library's device code is loaded there
+ * (with lazy module loading, the first use of it on that GPU) until the
+ * process exits.  Plans whose workspace_bytes exceed 16 MiB are rejected with
+ * ATTN_ERR_WORKSPACE_TOO_SMALL.  It allocates nothing (no cudaMalloc /
+ * cudaFree): each call uploads the work list with cudaMemcpyAsync from the
+ * plan's host memory (pageable, so the call returns once the copy has been
+ * staged, which may wait for earlier work on `stream`) and zeroes the counters
+ * and the error word with cudaMemsetAsync on `stream`, then launches the
+ * decode kernel.  The results are bit-identical to attn_decode's on the same
+ * plan and inputs.
  *
  * The first call on a device resolves the array's device address
  * (cudaGetSymbolAddress, with that device current); make that first call
  * before any stream capture.  All calls share the one array and it keeps the
  * last call's contents, so calls that overlap on the GPU (other streams, other
- * host threads) race: serialise them.  Device-side error bits of this path
- * are not reported (attn_plan_device_error reads the bound workspace only);
- * bad page ids are still skipped rather than read.
+ * host threads) race: serialise them.  Bad page ids are skipped rather than
+ * read and, like bounded-wait timeouts, set bits of the array's error word:
+ * read it with attn_decode_noalloc_device_error.
  */
 ATTN_API attn_status attn_decode_noalloc(attn_plan_t plan, const void* q, const void* kv_cache,
                                          const float* sinks, void* out, float* lse, void* stream);
+
+/*
+ * attn_decode_noalloc_device_error -- wait for `stream`, then read and clear
+ * the device error word (ATTN_DEVICE_ERR_* bits) that attn_decode_noalloc
+ * calls with this plan's layout left in the current device's static array,
+ * into *code.  Returns ATTN_ERR_DEVICE if any bit was set, ATTN_ERR_INVALID_ARG
+ * for a NULL argument or a graph plan.  The array is shared by every call, so
+ * read it before another call on the device may overwrite it.
+ */
+ATTN_API attn_status attn_decode_noalloc_device_error(attn_plan_t plan, int32_t* code, void* stream);
 
 /*
  * attn_graph_plan / attn_decode_graph -- decode that can be captured in a CUDA
@@ -368,6 +384,23 @@ ATTN_API const char* attn_status_string(attn_status status);
  * fails.
  */
 ATTN_API attn_status attn_selftest_bounded_wait(int64_t* result, void* stream);
+
+/*
+ * attn_selftest_exp2 -- diagnostic of the prefill softmax's exponentials.
+ * The online softmax of "GPT-OSS on day 0" (Perplexity), section "Sink
+ * Attention", needs exp(s - m) for every visible score; the prefill kernel
+ * evaluates it as 2^(s * sm_scale * log2(e) - m) and takes part of each
+ * tile's exponentials as a cubic polynomial on the FMA pipe instead of the
+ * MUFU's ex2.approx.  This launches, on `stream`, the kernel's own inline
+ * polynomial (with the kernel's argument set-up) next to ex2.approx:
+ *   y_poly[k] = polynomial 2^(x[k] * scale_log2 - m)   (argument clamped to [-126, 126])
+ *   y_mufu[k] = ex2.approx.ftz(x[k] * scale_log2 - m)
+ *   x, y_poly, y_mufu   DEVICE fp32 [n], caller-owned
+ * Returns ATTN_ERR_INVALID_ARG for n < 0 or NULL arrays (n > 0), ATTN_ERR_CUDA
+ * if the launch fails.  Allocates nothing.
+ */
+ATTN_API attn_status attn_selftest_exp2(const float* x, float* y_poly, float* y_mufu, int64_t n,
+                                        float scale_log2, float m, void* stream);
 
 #ifdef __cplusplus
 }

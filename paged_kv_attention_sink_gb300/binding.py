@@ -54,6 +54,7 @@ def _declare(lib):
         "attn_decode": (st, [p, p, p, p, p, p, p]),
         "attn_prefill": (st, [p, p, p, p, p, p, p]),
         "attn_decode_noalloc": (st, [p, p, p, p, p, p, p]),
+        "attn_decode_noalloc_device_error": (st, [p, p, p]),
         "attn_merge_states": (st, [p, p, p, p, p, p, i32, i32, i32, p]),
         "attn_append_kv": (st, [p, p, p, p, p]),
         "attn_plan_ragged": (st, [p, p, i32, i32, i32, i32, i32, f32, i32, p, p]),
@@ -70,6 +71,7 @@ def _declare(lib):
         "attn_plan_destroy": (None, [p]),
         "attn_status_string": (ctypes.c_char_p, [st]),
         "attn_selftest_bounded_wait": (st, [p, p]),
+        "attn_selftest_exp2": (st, [p, p, p, i64, f32, f32, p]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -445,3 +447,15 @@ def attn_selftest_bounded_wait(result=None, stream=None):
     _check("attn_selftest_bounded_wait", load_library().attn_selftest_bounded_wait(_ptr(result),
                                                                                    _stream_ptr(stream)))
     return result
+
+
+def attn_selftest_exp2(x, scale_log2=1.0, m=0.0, stream=None):
+    """Evaluate the prefill softmax's FMA-pipe 2^(x * scale_log2 - m) and the
+    MUFU's ex2.approx on the same fp32 CUDA tensor; returns (y_poly, y_mufu)."""
+    if not (isinstance(x, torch.Tensor) and x.is_cuda and x.dtype == torch.float32 and x.is_contiguous()):
+        raise TypeError("x must be a contiguous float32 CUDA tensor")
+    y_poly = torch.empty_like(x)
+    y_mufu = torch.empty_like(x)
+    _check("attn_selftest_exp2", load_library().attn_selftest_exp2(
+        _ptr(x), _ptr(y_poly), _ptr(y_mufu), x.numel(), float(scale_log2), float(m), _stream_ptr(stream)))
+    return y_poly, y_mufu
