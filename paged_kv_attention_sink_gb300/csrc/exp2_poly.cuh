@@ -15,8 +15,9 @@
 //     score's own fma: y = sat(s * (scale_log2 / R) + (1/2 - m / R)), so
 //     x' = R * y - R / 2 is x clamped to [-126, 126] (NaN clamps to -126).
 //     The clamp keeps the exponent arithmetic of step 4 inside the normal
-//     range (a result below 2^-126 is at most 2^-126 instead of 0; the
-//     softmax never asks for more than 2^8 here).
+//     range: a result below 2^-126 is at most 2^-126 instead of 0, and one
+//     above 2^126 is 2^126, large enough to trip the prefill softmax's
+//     row-sum check (2^64) that raises the running max and recomputes.
 //  2. Range reduction (Cody-Waite for base 2: the split is exact).
 //     t = fma_rm(y, R, C) with C = 1.5 * 2^23 - R / 2: the sum is exact in the
 //     fma and rounding toward -inf at a magnitude where one ulp is 1 leaves

@@ -28,11 +28,10 @@
 //    At D = 128, P is read from tensor memory where S was.
 //  * warps 4-7 / 8-11: softmax of head 0 / head 1, one thread per query row
 //    (= TMEM lane).  Causal / length mask on diagonal and ragged tiles only;
-//    the first tile of an item sets the running max, a later tile raises it
-//    only when its own row max is more than kRaise above (then O is rescaled
-//    in TMEM first), so every P is final after one pass; P is rounded to bf16
-//    and O is normalised by the row sum of that rounded P, while lse uses the
-//    unrounded sum.  At
+//    the row max is taken on an item's first tile only; later tiles keep it
+//    unless their P row sum passes 2^64 (then the max is raised, O rescaled in
+//    TMEM and the tile recomputed); P is rounded to bf16 and O is normalised
+//    by the row sum of that rounded P, while lse uses the unrounded sum.  At
 //    D = 64 a full 128-row tile's O leaves through the head slot's P buffer
 //    in shared memory and one TMA store; ragged last tiles use plain stores.
 //
@@ -52,11 +51,10 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-// A later tile raises the running max only when its row max exceeds it by
-// more than this (log2 units), so P stays below 2^kRaise.
-constexpr float kRaise = 8.0f;
+constexpr float kSumLimit = 18446744073709551616.0f;   // 2^64: tile row sum that forces a new max
 // Every kPolyEvery-th pair of score columns takes its exponentials on the FMA
-// pipe (exp2_poly.cuh) instead of the MUFU; 0 = none.
+// pipe (exp2_poly.cuh) instead of the MUFU; 0 = none.  The polynomial clamps
+// its argument to 2^126, which still trips the 2^64 row-sum check below.
 #ifndef ATTN_PREFILL_POLY_EVERY
 #define ATTN_PREFILL_POLY_EVERY 0
 #endif
@@ -125,7 +123,6 @@ struct Bars {
 __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity) {
     return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity));
 }
-
 
 // kRagged: K and V are contiguous [tokens][Hkv][D] arrays (kv_map over K,
 // v_map over V) instead of the paged HND pool (kv_map; v_map unused), and an
@@ -560,73 +557,44 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                     for (int c = 0; c < 128; ++c)
                         if (c >= ncol) s[c] = -INFINITY;
                 }
-                // Row max (log2 units): 16 independent chains of 3-input max,
-                // then a tree.  It runs before this warp takes its turn, on the
-                // ALU pipe, while the other head's warp has the MUFU.
-                float tmax;
-                {
+                // Row max: 16 independent chains of 3-input max, then a tree.
+                auto row_max = [&]() {
                     float mq[16];
 #pragma unroll
                     for (int k = 0; k < 16; ++k)
                         mq[k] = ptx::max3(ptx::max3(s[k], s[16 + k], s[32 + k]),
-                                          ptx::max3(s[48 + k], s[64 + k], s[80 + k]), fmaxf(s[96 + k], s[112 + k]));
+                                          ptx::max3(s[48 + k], s[64 + k], s[80 + k]),
+                                          ptx::max3(s[96 + k], s[112 + k], s[112 + k]));
 #pragma unroll
                     for (int k = 0; k < 5; ++k) mq[k] = ptx::max3(mq[k], mq[5 + k], mq[10 + k]);
-                    tmax = ptx::max3(ptx::max3(mq[0], mq[1], mq[2]), mq[3], fmaxf(mq[4], mq[15])) * sl2;
-                }
-                // The first tile of an item sets the running max.  A later
-                // tile raises it only when its own row max is more than kRaise
-                // above (any max is a valid softmax shift, so P = 2^(s - m) may
-                // reach 2^kRaise); then the state so far, O included, is
-                // rescaled.  Every P of the tile is final after one pass, so
-                // the scores need not outlive the exponentials.
+                    return ptx::max3(ptx::max3(mq[0], mq[1], mq[2]), ptx::max3(mq[3], mq[4], mq[15]), mq[15]);
+                };
+                // Raise the running max to cover this tile; returns the factor
+                // that rescales the state accumulated so far.
+                auto raise_max = [&]() {
+                    const float m_new = fmaxf(m_use, row_max() * sl2);
+                    const float alpha = m_new > m_use ? ptx::ex2(m_use - m_new) : 1.f;
+                    l *= alpha;
+                    le *= alpha;
+                    m_use = m_new;
+                    return alpha;
+                };
+                // The first tile of an item sets the running max.  Later tiles
+                // reuse it and skip the max: P = 2^(s - m) is computed directly,
+                // and only when the tile's row sum exceeds 2^64 (some P could
+                // then be large enough to overflow the sums) is the max raised,
+                // O rescaled and the tile recomputed.  Any max is a valid
+                // softmax shift, so the result does not depend on when it moves.
+                if (j == 0) raise_max();
                 // At D = 64 the previous PV must be done before O is touched or
                 // P is overwritten (at D = 128 it is: S of tile j waited for it).
                 bool prev_done = !C::kSeparateP || t == 0;
-                if (j == 0) {
-                    if (tmax > m_use) {
-                        const float alpha = ptx::ex2(m_use - tmax);
-                        l *= alpha;
-                        le *= alpha;
-                        m_use = tmax;
-                    }
-                } else if (__any_sync(0xffffffffu, tmax > m_use + kRaise)) {
-                    float alpha = 1.f;
-                    if (tmax > m_use) {
-                        alpha = ptx::ex2(m_use - tmax);
-                        l *= alpha;
-                        le *= alpha;
-                        m_use = tmax;
-                    }
-                    if (!prev_done) {
-                        if (!wait_all(B.o_done + 8 * i, (t - 1) & 1)) { ok = false; break; }
-                        prev_done = true;
-                        ptx::tc_fence_after();
-                    }
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t v[32];
-                        ptx::tmem_ld32(t_o + c * 32, v);
-                        ptx::tc_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                        ptx::tmem_st32(t_o + c * 32, v);
-                    }
-                    if constexpr (C::kSplitP) {   // the row-sum columns
-                        uint32_t v[16];
-                        ptx::tmem_ld16(t_o + D, v);
-                        ptx::tc_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                        ptx::tmem_st16(t_o + D, v);
-                    }
-                    ptx::tc_wait_st();
-                }
                 uint32_t pk[2][32];
                 float tile_l = 0.f, tile_le = 0.f;
                 const bool take_turns = C::kSplitP && it.n_heads == 2;
                 if (take_turns && !wait_all(my_turn, n_turn & 1)) { ok = false; break; }
-                {
+#pragma unroll 1
+                for (int pass = 0;; ++pass) {
                     const float neg_m = m_use == -INFINITY ? 0.f : -m_use;
                     const float2 sl2x2 = make_float2(sl2, sl2), negm2 = make_float2(neg_m, neg_m);
                     // Pairs on the FMA pipe: y = sat(s * sl2 / R + 1/2 - m / R).
@@ -654,6 +622,30 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                     const float2 lsum = ptx::add2(ls2[0], ls2[1]), lxsum = ptx::add2(lx2[0], lx2[1]);
                     tile_l = lsum.x + lsum.y;
                     tile_le = lxsum.x + lxsum.y;
+                    if (j == 0 || pass > 0 || !__any_sync(0xffffffffu, tile_le > kSumLimit)) break;
+                    const float alpha = raise_max();
+                    if (!prev_done) {
+                        if (!wait_all(B.o_done + 8 * i, (t - 1) & 1)) { ok = false; break; }
+                        prev_done = true;
+                        ptx::tc_fence_after();
+                    }
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t v[32];
+                        ptx::tmem_ld32(t_o + c * 32, v);
+                        ptx::tc_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                        ptx::tmem_st32(t_o + c * 32, v);
+                    }
+                    if constexpr (C::kSplitP) {   // the row-sum columns
+                        uint32_t v[16];
+                        ptx::tmem_ld16(t_o + D, v);
+                        ptx::tc_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                        ptx::tmem_st16(t_o + D, v);
+                    }
                 }
                 if (take_turns) {
                     __syncwarp();
