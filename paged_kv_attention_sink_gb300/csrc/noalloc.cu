@@ -1,17 +1,18 @@
 // attn_decode_noalloc: attn_decode without a caller-allocated workspace.
 //
 // Some callers cannot allocate device memory at the point where they run
-// attention: an engine whose decode step is replayed from a captured CUDA
-// graph, or one that reserves its whole memory budget up front and forbids
-// cudaMalloc afterwards (whose implicit device synchronisation would also
-// stall every other stream).  attn_decode needs a workspace from the caller;
-// this variant instead uses a fixed scratch area compiled into the library.
+// attention: an engine that reserves its whole memory budget up front and
+// forbids cudaMalloc while it serves (cudaMalloc may also synchronise the
+// device and stall every other stream).  attn_decode needs a workspace from
+// the caller; this variant instead uses a fixed scratch area compiled into
+// the library.
 //
-// The scratch is one file-scope __device__ array of kNoAllocScratchBytes.
-// Every GPU on which the library's module is loaded holds it until the
-// process exits.  Host code cannot use the array's name as a device address,
-// so the first call on each device resolves it with cudaGetSymbolAddress
-// (with that device current) and caches the pointer.
+// The scratch is one file-scope __device__ array of kNoAllocScratchBytes.  A
+// GPU holds it from the moment the library's device code is loaded there
+// (with lazy module loading, the first use of this file's code on that GPU)
+// until the process exits.  Host code cannot use the array's name as a device
+// address, so the first call on each device resolves it with
+// cudaGetSymbolAddress (with that device current) and caches the pointer.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -56,6 +57,9 @@ extern "C" attn_status attn_decode_noalloc(attn_plan_t plan, const void* q, cons
                                            const float* sinks, void* out, float* lse,
                                            void* stream) {
     if (!plan) return ATTN_ERR_INVALID_ARG;
+    // A graph plan's work list is built on the device (attn_decode_graph);
+    // its host list is empty, so it must not pass for an empty batch.
+    if (plan->graph) return ATTN_ERR_INVALID_ARG;
     if (plan->units.empty()) return ATTN_OK;
     if (!q || !kv_cache || !out) return ATTN_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(kv_cache) |
@@ -79,4 +83,18 @@ extern "C" attn_status attn_decode_noalloc(attn_plan_t plan, const void* q, cons
     alignas(64) unsigned char map[128];
     if (!attn::encode_decode_kv_map(map, kv_cache, plan)) return ATTN_ERR_CUDA;
     return attn::launch_decode_scratch(plan, scratch, q, map, sinks, out, lse, s);
+}
+
+extern "C" attn_status attn_decode_noalloc_device_error(attn_plan_t plan, int32_t* code, void* stream) {
+    if (!plan || !code || plan->graph) return ATTN_ERR_INVALID_ARG;
+    const attn::WorkspaceLayout& L = plan->layout;
+    if (L.total > kNoAllocScratchBytes) return ATTN_ERR_WORKSPACE_TOO_SMALL;
+    unsigned char* scratch = scratch_on_current_device();
+    if (!scratch) return ATTN_ERR_CUDA;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+    int32_t v = 0;
+    if (cudaMemcpy(&v, scratch + L.err, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (v != 0 && cudaMemset(scratch + L.err, 0, sizeof v) != cudaSuccess) return ATTN_ERR_CUDA;
+    *code = v;
+    return v != 0 ? ATTN_ERR_DEVICE : ATTN_OK;
 }
