@@ -209,6 +209,23 @@ ATTN_API attn_status attn_merge_states(const void* va, const float* lsea, const 
                               int32_t n_heads, int32_t head_dim, void* stream);
 
 /*
+ * attn_merge_states_f32 -- the same log-sum-exp merge for fp32 value states:
+ * partial states kept unrounded (a KV sequence split across calls or
+ * devices, the sink counted in one part only, as in "GPT-OSS on day 0",
+ * section "Sink Attention") merge without rounding each part to bf16 first.
+ *   va, vb         fp32 [n_tokens][n_heads][head_dim], 16-byte aligned
+ *   lsea, lseb     fp32 [n_tokens][n_heads], natural log
+ *   vout           fp32 (vout_bf16 = 0; 16-byte aligned, may alias va or vb)
+ *                  or bf16 (vout_bf16 != 0; 8-byte aligned), [n_tokens][n_heads][head_dim]
+ *   lseout         fp32 [n_tokens][n_heads] or NULL
+ * head_dim a multiple of 4, at most 256.  Device pointers, async on stream;
+ * ATTN_ERR_INVALID_ARG for bad sizes, NULL or misaligned pointers.
+ */
+ATTN_API attn_status attn_merge_states_f32(const float* va, const float* lsea, const float* vb,
+                                           const float* lseb, void* vout, int32_t vout_bf16, float* lseout,
+                                           int32_t n_tokens, int32_t n_heads, int32_t head_dim, void* stream);
+
+/*
  * attn_decode_noalloc -- attn_decode for callers that cannot allocate device
  * memory when they run attention: an engine that reserves its whole memory
  * budget up front and forbids cudaMalloc while it serves (cudaMalloc may also

@@ -56,6 +56,7 @@ def _declare(lib):
         "attn_decode_noalloc": (st, [p, p, p, p, p, p, p]),
         "attn_decode_noalloc_device_error": (st, [p, p, p]),
         "attn_merge_states": (st, [p, p, p, p, p, p, i32, i32, i32, p]),
+        "attn_merge_states_f32": (st, [p, p, p, p, p, i32, p, i32, i32, i32, p]),
         "attn_append_kv": (st, [p, p, p, p, p]),
         "attn_plan_ragged": (st, [p, p, i32, i32, i32, i32, i32, f32, i32, p, p]),
         "attn_graph_plan": (st, [i32, i32, i32, i32, i32, f32, i32, i64, p, i32, p, p]),
@@ -398,6 +399,25 @@ def attn_merge_states(va, lsea, vb, lseb, vout=None, lseout=None, stream=None):
     _check("attn_merge_states", load_library().attn_merge_states(
         _ptr(va), _ptr(lsea), _ptr(vb), _ptr(lseb), _ptr(vout), _ptr(lseout), n, H, D,
         _stream_ptr(stream)))
+    return vout, lseout
+
+
+def attn_merge_states_f32(va, lsea, vb, lseb, vout=None, lseout=None, out_dtype=torch.float32, stream=None):
+    """Merge two (fp32 [n, H, D], fp32 [n, H]) attention states by log-sum-exp;
+    the merged values are fp32 or bf16 (out_dtype, or vout's dtype)."""
+    for name, t in (("va", va), ("vb", vb), ("lsea", lsea), ("lseb", lseb)):
+        if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.float32 and t.is_contiguous()):
+            raise TypeError(f"{name} must be a contiguous float32 CUDA tensor")
+    n, H, D = va.shape
+    if vb.shape != va.shape or lsea.shape != (n, H) or lseb.shape != (n, H):
+        raise ValueError("state shapes disagree")
+    if vout is None:
+        vout = torch.empty(n, H, D, dtype=out_dtype, device=va.device)
+    if vout.dtype not in (torch.float32, torch.bfloat16) or vout.shape != va.shape or not vout.is_contiguous():
+        raise TypeError("vout must be a contiguous float32 or bfloat16 tensor shaped like va")
+    _check("attn_merge_states_f32", load_library().attn_merge_states_f32(
+        _ptr(va), _ptr(lsea), _ptr(vb), _ptr(lseb), _ptr(vout), int(vout.dtype == torch.bfloat16), _ptr(lseout),
+        n, H, D, _stream_ptr(stream)))
     return vout, lseout
 
 

@@ -226,7 +226,22 @@ extern "C" attn_status attn_merge_states(const void* va, const float* lsea, cons
          reinterpret_cast<uintptr_t>(vout)) & 7)
         return ATTN_ERR_INVALID_ARG;
     return attn::launch_merge_states(va, lsea, vb, lseb, vout, lseout, (int64_t)n_tokens * n_heads,
-                                     head_dim, static_cast<cudaStream_t>(stream));
+                                     head_dim, false, false, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" attn_status attn_merge_states_f32(const float* va, const float* lsea, const float* vb,
+                                             const float* lseb, void* vout, int32_t vout_bf16, float* lseout,
+                                             int32_t n_tokens, int32_t n_heads, int32_t head_dim, void* stream) {
+    if (n_tokens < 0 || n_heads <= 0 || head_dim <= 0 || head_dim % 4 != 0 || head_dim > 256)
+        return ATTN_ERR_INVALID_ARG;
+    if (n_tokens == 0) return ATTN_OK;
+    if (!va || !lsea || !vb || !lseb || !vout) return ATTN_ERR_INVALID_ARG;
+    const uintptr_t out_align = vout_bf16 ? 7 : 15;
+    if (((reinterpret_cast<uintptr_t>(va) | reinterpret_cast<uintptr_t>(vb)) & 15) ||
+        (reinterpret_cast<uintptr_t>(vout) & out_align))
+        return ATTN_ERR_INVALID_ARG;
+    return attn::launch_merge_states(va, lsea, vb, lseb, vout, lseout, (int64_t)n_tokens * n_heads, head_dim, true,
+                                     vout_bf16 == 0, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" attn_status attn_append_kv(attn_plan_t plan, const void* k_new, const void* v_new, void* kv_cache,

@@ -15,9 +15,10 @@ attn_status launch_decode(attn_plan_s* plan, const void* q, const void* kv_map, 
 // through it).
 attn_status launch_prefill(attn_plan_s* plan, const void* q_map, const void* kv_map, const void* v_map,
                            const void* o_map, const float* sinks, void* out, float* lse, cudaStream_t stream);
-attn_status launch_merge_states(const void* va, const float* lsea, const void* vb,
-                                const float* lseb, void* vout, float* lseout, int64_t rows,
-                                int head_dim, cudaStream_t stream);
+// in_f32 / out_f32: value states / merged values are fp32 (else bf16).
+attn_status launch_merge_states(const void* va, const float* lsea, const void* vb, const float* lseb, void* vout,
+                                float* lseout, int64_t rows, int head_dim, bool in_f32, bool out_f32,
+                                cudaStream_t stream);
 // CUDA-graph decode: device planner + persistent decode over its work list.
 attn_status launch_decode_graph(attn_plan_s* plan, const int32_t* kv_indptr, const int32_t* last_page_len,
                                 const int32_t* batch, const void* q, const void* kv_map, const float* sinks,

@@ -200,11 +200,34 @@ def test_launch_without_workspace_is_rejected(lib):
     lib.attn_plan_destroy(h)
 
 
+def test_noalloc_decode_refuses_graph_plans(lib):
+    """A graph plan's work list is built on the device, so its host list is
+    empty; the no-alloc decode must refuse it rather than report an empty
+    batch as done.  Neither call reaches the device here."""
+    h = ctypes.c_void_p()
+    ws = ctypes.c_size_t()
+    assert lib.attn_graph_plan(8, 16, 2, 64, 16, ctypes.c_float(0.125), 1024, 8 * 4096, ctypes.c_void_p(0x10000),
+                               152, ctypes.byref(h), ctypes.byref(ws)) == OK
+    dummy = ctypes.c_void_p(0x10000)
+    assert lib.attn_decode_noalloc(h, dummy, dummy, None, dummy, None, None) == INVALID
+    code = ctypes.c_int32(-1)
+    assert lib.attn_decode_noalloc_device_error(h, ctypes.byref(code), None) == INVALID
+    assert lib.attn_decode_noalloc(None, dummy, dummy, None, dummy, None, None) == INVALID
+    assert lib.attn_decode_noalloc_device_error(None, ctypes.byref(code), None) == INVALID
+    lib.attn_plan_destroy(h)
+
+
 def test_merge_states_argument_checks(lib):
     p = ctypes.c_void_p(0x10000)
     assert lib.attn_merge_states(p, p, p, p, p, None, 4, 2, 6, None) == INVALID   # D % 4
     assert lib.attn_merge_states(p, p, p, p, p, None, -1, 2, 8, None) == INVALID
     assert lib.attn_merge_states(None, None, None, None, None, None, 0, 2, 8, None) == OK
+    # fp32 states: 16-byte aligned inputs, 16 (fp32) or 8 (bf16) byte aligned output
+    assert lib.attn_merge_states_f32(p, p, p, p, p, 0, None, 4, 2, 6, None) == INVALID   # D % 4
+    assert lib.attn_merge_states_f32(p, p, p, p, ctypes.c_void_p(0x10008), 0, None, 4, 2, 8, None) == INVALID
+    assert lib.attn_merge_states_f32(ctypes.c_void_p(0x10008), p, p, p, p, 0, None, 4, 2, 8, None) == INVALID
+    assert lib.attn_merge_states_f32(None, None, None, None, None, 1, None, 0, 2, 8, None) == OK
+    assert lib.attn_merge_states_f32(None, p, p, p, p, 1, None, 4, 2, 8, None) == INVALID
 
 
 def test_head_slice_argument_checks(lib):
