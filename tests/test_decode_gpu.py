@@ -58,15 +58,13 @@ def test_gptoss_decode_full():
     check_close(out, lse, ref_out, ref_lse, "gpt-oss decode")
 
 
-def test_qwen_decode_full_sampled():
+def test_qwen_decode_full():
+    """All 128 requests x 64 heads of the Qwen3-shaped long-context decode
+    (kv_len log-uniform in [2048, 32768], no sinks) against the oracle."""
     batch = syn.qwen_decode(0)
     out, lse, _ = run_decode(batch)
-    rows, heads = sample_pairs(batch, decode_rows(batch), 384, seed=3)
-    ref_out, ref_lse = oracle.sink_attention(batch, rows=rows, heads=heads)
-    o = out[torch.from_numpy(rows).cuda(), torch.from_numpy(heads).long().cuda()]
-    l = lse[torch.from_numpy(rows).cuda(), torch.from_numpy(heads).long().cuda()]
-    check_close(o, l, ref_out, ref_lse, "qwen decode")
-    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+    ref_out, ref_lse = oracle.sink_attention(batch)
+    check_close(out, lse, ref_out, ref_lse, "qwen decode")
 
 
 @pytest.mark.parametrize("Hq,Hkv,D,P", [

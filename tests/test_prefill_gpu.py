@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import oracle
-from helpers import check_close, make_plan, prefill_rows, sample_pairs, syn, to_device
+from helpers import check_close, make_plan, prefill_rows, syn, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -113,19 +113,19 @@ def test_prefill_max_jumps_past_sum_limit(causal):
     _check_rows(batch, out, lse, what=f"max jump causal={causal}")
 
 
-def test_gptoss_prefill_full_sampled():
+def test_gptoss_prefill_full():
+    """Every row and head of the gpt-oss-shaped prefill (13,804 rows x 64
+    heads, 3,584 work items over 152 persistent CTAs) against the oracle, in
+    the launch configuration the benchmark times."""
     batch = syn.gptoss_prefill(0)
     out, lse, plan = run_prefill(batch)
-    rows, heads = sample_pairs(batch, prefill_rows(batch), 512, seed=1)
-    ref_out, ref_lse = oracle.sink_attention(batch, rows=rows, heads=heads)
-    ri = torch.from_numpy(rows).cuda()
-    hi = torch.from_numpy(heads).long().cuda()
-    check_close(out[ri, hi], lse[ri, hi], ref_out, ref_lse, "gpt-oss prefill")
-    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+    ref_out, ref_lse = oracle.sink_attention(batch)
+    check_close(out, lse, ref_out, ref_lse, "gpt-oss prefill")
 
 
-def test_mixed_batch_full_sampled():
-    """One plan, prefill then decode on the same stream."""
+def test_mixed_batch_full():
+    """One plan, prefill then decode on the same stream; every row and head
+    (8,192 prefill rows and 256 decode rows x 64 heads) against the oracle."""
     batch = syn.mixed(0)
     q, kv, pt, sk = to_device(batch)
     plan = make_plan(batch, pt)
@@ -135,13 +135,8 @@ def test_mixed_batch_full_sampled():
     plan.decode(q, kv, sk, out, lse)
     torch.cuda.synchronize()
     assert plan.device_error() == 0
-    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
-    all_rows = list(range(batch.total_rows))
-    rows, heads = sample_pairs(batch, all_rows, 768, seed=2)
-    ref_out, ref_lse = oracle.sink_attention(batch, rows=rows, heads=heads)
-    ri = torch.from_numpy(rows).cuda()
-    hi = torch.from_numpy(heads).long().cuda()
-    check_close(out[ri, hi], lse[ri, hi], ref_out, ref_lse, "mixed")
+    ref_out, ref_lse = oracle.sink_attention(batch)
+    check_close(out, lse, ref_out, ref_lse, "mixed")
 
 
 def test_prefill_bitwise_deterministic():
@@ -174,19 +169,12 @@ def test_prefill_persistent_item_streams(num_sms):
     _check_rows(batch, out, lse, what=f"sms={num_sms}")
 
 
-def test_prefill_long_sequence_sampled():
+def test_prefill_long_sequence_full():
     """A 32K-token sequence whose last 8K tokens are the prefill rows (24K cached
     prefix), Qwen3-like D = 128 and P = 64: 256 KV tiles per item, so the
-    running max is reused across many tiles and the item lists are long.  The
-    first and last rows of the long request are always checked."""
+    running max is reused across many tiles and the item lists are long.
+    Every row and head against the oracle."""
     batch = syn.make_batch("long", [8192, 300], [32768, 300], 16, 4, 128, 64, seed=13)
     out, lse, _ = run_prefill(batch)
-    rows, heads = sample_pairs(batch, prefill_rows(batch), 384, seed=3)
-    edge = np.array([0, 0, 8191, 8191, 8192, 8491], dtype=np.int64)
-    rows = np.concatenate([rows, edge])
-    heads = np.concatenate([heads, np.array([0, 15, 3, 12, 7, 8], dtype=np.int32)])
-    ref_out, ref_lse = oracle.sink_attention(batch, rows=rows, heads=heads)
-    ri = torch.from_numpy(rows).cuda()
-    hi = torch.from_numpy(heads).long().cuda()
-    check_close(out[ri, hi], lse[ri, hi], ref_out, ref_lse, "long prefill")
-    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+    ref_out, ref_lse = oracle.sink_attention(batch)
+    check_close(out, lse, ref_out, ref_lse, "long prefill")
