@@ -66,6 +66,18 @@ def kv_bytes(batch, rows_only=None):
     return int(np.sum(kv)) * per_tok
 
 
+def sample_prefill_flops(batch, rows):
+    """Algorithmic flops of the given query rows (all heads): 4 * D per
+    visible (query, key) pair per head, as prefill_flops counts them."""
+    pairs = 0
+    for r in rows:
+        b = int(np.searchsorted(batch.qo_indptr, r, side="right") - 1)
+        qo, kv = int(batch.qo_lens[b]), int(batch.kv_lens[b])
+        i = int(r - batch.qo_indptr[b])
+        pairs += min(kv, kv - qo + i + 1) if batch.causal else kv
+    return pairs * batch.num_qo_heads * 4 * batch.head_dim
+
+
 def prefill_flops(batch):
     pairs = 0
     for b in range(batch.batch_size):
@@ -86,7 +98,7 @@ class NvmlSampler:
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, uuid: str, period_s: float = 0.002):
+    def __init__(self, uuid: str, period_s: float = 0.0005):
         self.uuid, self.period = uuid, period_s
         self.samples, self.thread, self.stop_flag = [], None, False
         self.nvml = self.handle = None
@@ -235,6 +247,16 @@ def job_throughput(bytes_per_rank_step, steps, rank_seconds, world):
     return world * bytes_per_rank_step * steps / max_over_ranks(rank_seconds, world) / 1e9
 
 
+def headline_config(batch, world):
+    """The headline workload, as both arms report it (static: no timings)."""
+    return {"workload": "gptoss_decode", "batch": batch.batch_size, "kv_len": "U[1024,8192]",
+            "Hq": batch.num_qo_heads, "Hkv": batch.num_kv_heads, "head_dim": batch.head_dim,
+            "page_size": batch.page_size, "split_kv": True, "sinks": batch.sinks is not None,
+            "kv_bytes_per_step": kv_bytes(batch),
+            "l2": "flushed before every timed step (256 MB memset, then a 256 MB read: cold L2, no dirty lines)",
+            "parallelism": f"replicas x{world}"}
+
+
 # ----------------------------------------------------------- reference arm
 def run_reference(args, world, rank):
     if rank != 0:
@@ -262,8 +284,7 @@ def run_reference(args, world, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": "gptoss_decode", "batch": batch.batch_size, "Hq": 64, "Hkv": 8,
-                   "head_dim": 64, "page_size": 16, "kv_len": "U[1024,8192]"},
+        "config": headline_config(batch, world),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -301,6 +322,19 @@ class L2Flush:
         self.w.zero_()
         self.r.sum()
 
+
+
+def leg_steps(args):
+    """Launches timed by each side leg: at least 50, whatever --steps says."""
+    return max(50, args.steps // 10)
+
+
+def timed_leg(fn, steps, flush, stream, gpu_id):
+    """time_device with an NVML clock record of its own."""
+    sampler = NvmlSampler(gpu_id)
+    sampler.start()
+    times = time_device(fn, steps, flush, stream)
+    return times, sampler.stop()
 
 
 def time_device(fn, steps, flush, stream):
@@ -409,15 +443,15 @@ def run_ours(args, world, rank, local):
         torch.cuda.current_stream().wait_stream(cs)
         for _ in range(args.warmup):
             cg.replay()
-        gsteps = max(3, args.steps // 10)
-        gtimes = time_device(cg.replay, gsteps, flush, stream)
+        gsteps = leg_steps(args)
+        gtimes, gclocks = timed_leg(cg.replay, gsteps, flush, stream, gpu_id)
         gmean = sum(gtimes) / len(gtimes) / 1e3
         if gplan.device_error():
             raise RuntimeError("graph decode recorded a device error")
         graph = {"workload": "gptoss_decode, one CUDA-graph replay (device planner + persistent decode)",
                  "value": bytes_step / gmean / 1e9, "unit": "GB/s", "ms_per_step": gmean * 1e3,
                  "frac_of_hbm_peak": bytes_step / gmean / 1e9 / float(peaks["hbm_gbs"]),
-                 "launches": 2 * gsteps}
+                 "steps": gsteps, "launches": 2 * gsteps, "clocks": gclocks}
     except binding.AttnError as e:
         graph = {"unavailable": str(e)}
 
@@ -450,7 +484,10 @@ def run_ours(args, world, rank, local):
             "res_h": torch.empty(out_bytes + lse_bytes, dtype=torch.uint8).pin_memory(),
             "ev": torch.cuda.Event(), "uploaded": torch.cuda.Event(), "decoded": torch.cuda.Event(),
             "plan": None, "ws": torch.empty(plan.info()["workspace_bytes"], dtype=torch.uint8, device=dev)})
-    e2e_steps = max(3, min(args.steps, 200))
+    # A fixed 500 steps (about 50 ms), whatever --steps says: with three steps
+    # in flight, a short region is dominated by filling and draining the
+    # pipeline.
+    e2e_steps = 500
     up_stream, down_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     torch.cuda.synchronize()   # the slots' buffers exist before other streams touch them
 
@@ -508,14 +545,18 @@ def run_ours(args, world, rank, local):
             for _ in range(args.warmup):
                 pre()
             torch.cuda.synchronize()
-            psteps = max(3, args.steps // 10)
-            ptimes = time_device(pre, psteps, flush, stream)
+            psteps = leg_steps(args)
+            ptimes, pclocks = timed_leg(pre, psteps, flush, stream, gpu_id)
             pmean = sum(ptimes) / len(ptimes) / 1e3
             flops = prefill_flops(pbatch)
             tf = flops / pmean / 1e12
             ppeak = float(peaks["bf16_tflops"])
+            mhz = pclocks.get("sm_mhz")
             prefill = {"workload": "gptoss_prefill", "value": tf, "unit": "TFLOP/s",
-                       "ms_per_step": pmean * 1e3, "steps": psteps,
+                       "ms_per_step": pmean * 1e3, "steps": psteps, "clocks": pclocks,
+                       # time x median SM clock: the launch in SM cycles, comparable across clocks
+                       "sm_cycles_per_step": pmean * mhz * 1e6 if mhz else None,
+                       "flops": flops,
                        "roofline": {"bound": "tensor", "achieved": tf, "peak": ppeak,
                                     "unit": "TFLOP/s", "frac": tf / ppeak,
                                     "traffic": traffic_for("prefill.cu", "prefill_gptoss"),
@@ -540,12 +581,13 @@ def run_ours(args, world, rank, local):
         rag = lambda: rplan.prefill(pq, rk, rv, psk, pout, plse)
         for _ in range(args.warmup):
             rag()
-        rsteps = max(3, args.steps // 10)
-        rtimes = time_device(rag, rsteps, flush, stream)
+        rsteps = leg_steps(args)
+        rtimes, rclocks = timed_leg(rag, rsteps, flush, stream, gpu_id)
         rmean = sum(rtimes) / len(rtimes) / 1e3
         rtf = prefill_flops(pbatch) / rmean / 1e12
         ragged = {"workload": "gptoss_prefill, contiguous K/V (no cache)", "value": rtf, "unit": "TFLOP/s",
-                  "ms_per_step": rmean * 1e3, "frac_of_bf16_peak": rtf / float(peaks["bf16_tflops"])}
+                  "ms_per_step": rmean * 1e3, "frac_of_bf16_peak": rtf / float(peaks["bf16_tflops"]),
+                  "steps": rsteps, "clocks": rclocks}
         launches += rsteps
 
     # ---- KV-cache legs (HBM copies): the step's append on the prefill batch,
@@ -558,8 +600,8 @@ def run_ours(args, world, rank, local):
         app = lambda: pplan.append_kv(kd, vd, pkv)
         for _ in range(args.warmup):
             app()
-        asteps = max(3, args.steps // 10)
-        atimes = time_device(app, asteps, flush, stream)
+        asteps = leg_steps(args)
+        atimes, aclocks = timed_leg(app, asteps, flush, stream, gpu_id)
         amean = sum(atimes) / len(atimes) / 1e3
         abytes = 2 * 2 * kd.numel() * 2                       # K and V rows, read once + written once
         ids = torch.from_numpy(np.unique(batch.page_table)).to(dev)
@@ -568,17 +610,18 @@ def run_ours(args, world, rank, local):
         pk = lambda: binding.attn_pack_kv_heads(kv, ids, 0, nh, buf=buf)
         for _ in range(args.warmup):
             pk()
-        ktimes = time_device(pk, asteps, flush, stream)
+        ktimes, kclocks = timed_leg(pk, asteps, flush, stream, gpu_id)
         kmean = sum(ktimes) / len(ktimes) / 1e3
         kbytes = 2 * buf.numel() * 2                           # slice read once + buffer written once
         peak = float(peaks["hbm_gbs"])
         kvcache = {
             "append": {"workload": "gptoss_prefill rows (new K/V of every query row)", "bytes": abytes,
                        "us": amean * 1e6, "value": abytes / amean / 1e9, "unit": "GB/s",
-                       "frac_of_hbm_peak": abytes / amean / 1e9 / peak},
+                       "frac_of_hbm_peak": abytes / amean / 1e9 / peak, "steps": asteps, "clocks": aclocks},
             "pack_heads": {"workload": f"gptoss_decode pool, heads [0,{nh}) of {ids.numel()} pages",
                            "bytes": kbytes, "us": kmean * 1e6, "value": kbytes / kmean / 1e9, "unit": "GB/s",
-                           "frac_of_hbm_peak": kbytes / kmean / 1e9 / peak},
+                           "frac_of_hbm_peak": kbytes / kmean / 1e9 / peak, "steps": asteps,
+                           "clocks": kclocks},
         }
         launches += 2 * asteps
 
@@ -590,7 +633,7 @@ def run_ours(args, world, rank, local):
         others = {}
         hbm = float(peaks["hbm_gbs"])
         tc = float(peaks["bf16_tflops"])
-        osteps = max(3, args.steps // 10)
+        osteps = leg_steps(args)
         def pool_on_device(b_):
             # N(0,1) bf16, drawn on the GPU (seeded): these legs only time kernels
             g = torch.Generator(device=dev)
@@ -617,14 +660,14 @@ def run_ours(args, world, rank, local):
         qdec = lambda: qplan.decode(qq, qkv, qsk, qout, qlse)
         for _ in range(args.warmup):
             qdec()
-        qtimes = time_device(qdec, osteps, flush, stream)
+        qtimes, qclocks = timed_leg(qdec, osteps, flush, stream, gpu_id)
         qmean = sum(qtimes) / len(qtimes) / 1e3
         qbytes = kv_bytes(qb)
         others["qwen_decode"] = {
             "workload": "qwen_decode: 128 requests, kv_len log-U[2048,32768], Hq 64, Hkv 4, D 128, P 64, no sinks"
                         " (KV pool drawn on the GPU)",
             "bytes": qbytes, "ms_per_step": qmean * 1e3, "value": qbytes / qmean / 1e9, "unit": "GB/s",
-            "frac_of_hbm_peak": qbytes / qmean / 1e9 / hbm}
+            "frac_of_hbm_peak": qbytes / qmean / 1e9 / hbm, "steps": osteps, "clocks": qclocks}
         launches += osteps
         del qq, qkv, qpt, qout, qlse, qplan
         mb = syn.mixed(seed=rank, fill_pool=False)
@@ -637,9 +680,9 @@ def run_ours(args, world, rank, local):
         for _ in range(args.warmup):
             mpre()
             mdec()
-        mp = time_device(mpre, osteps, flush, stream)
-        md = time_device(mdec, osteps, flush, stream)
-        mboth = time_device(lambda: (mpre(), mdec()), osteps, flush, stream)
+        mp, mpclocks = timed_leg(mpre, osteps, flush, stream, gpu_id)
+        md, mdclocks = timed_leg(mdec, osteps, flush, stream, gpu_id)
+        mboth, mbclocks = timed_leg(lambda: (mpre(), mdec()), osteps, flush, stream, gpu_id)
         mp_s, md_s, mb_s = (sum(t) / len(t) / 1e3 for t in (mp, md, mboth))
         mflops, mbytes = prefill_flops(mb), kv_bytes(mb)
         ideal = mflops / (tc * 1e12) + mbytes / (hbm * 1e9)
@@ -648,7 +691,8 @@ def run_ours(args, world, rank, local):
                         " (KV pool drawn on the GPU)",
             "prefill_tflops": mflops / mp_s / 1e12, "prefill_frac_of_bf16_peak": mflops / mp_s / 1e12 / tc,
             "decode_gbs": mbytes / md_s / 1e9, "decode_frac_of_hbm_peak": mbytes / md_s / 1e9 / hbm,
-            "both_ms": mb_s * 1e3, "combined_frac_of_ideal": ideal / mb_s}
+            "both_ms": mb_s * 1e3, "combined_frac_of_ideal": ideal / mb_s, "steps": osteps,
+            "clocks": {"prefill": mpclocks, "decode": mdclocks, "both": mbclocks}}
         launches += 4 * osteps
         del mq, mkv, mpt, mout, mlse, mplan
 
@@ -666,6 +710,35 @@ def run_ours(args, world, rank, local):
         dt = time.perf_counter() - t0
         cpu = {"value": bytes_step / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
                "sample": f"the whole gptoss_decode batch (seed 0), fp64 C oracle, {dt:.2f} s"}
+        # One core: the tiny decode whole, and 1/64 of the headline batch
+        # (request 0, all 64 heads).
+        tiny = syn.tiny_decode(0)
+        t0 = time.perf_counter()
+        oracle.sink_attention(tiny, n_threads=1)
+        dt_tiny = time.perf_counter() - t0
+        r1, h1 = np.zeros(batch.num_qo_heads, dtype=np.int64), np.arange(batch.num_qo_heads, dtype=np.int32)
+        t0 = time.perf_counter()
+        oracle.sink_attention(batch, rows=r1, heads=h1, n_threads=1)
+        dt_one = time.perf_counter() - t0
+        cpu["single_core"] = {
+            "tiny_decode": {"value": kv_bytes(tiny) / dt_tiny / 1e9, "unit": "GB/s", "seconds": dt_tiny},
+            "gptoss_decode_1_64": {"value": kv_bytes(batch, rows_only=batch.kv_lens[:1]) / dt_one / 1e9,
+                                   "unit": "GB/s", "seconds": dt_one,
+                                   "sample": "request 0 of the gptoss_decode batch, all 64 heads"}}
+        # Prefill: every 64th query row of the gpt-oss prefill, all heads, on
+        # all cores; the throughput of that sample estimates the whole run.
+        if not args.no_prefill and prefill is not None and "unavailable" not in prefill:
+            prow = np.arange(0, pbatch.total_rows, 64, dtype=np.int64)
+            pr = np.repeat(prow, pbatch.num_qo_heads)
+            ph = np.tile(np.arange(pbatch.num_qo_heads, dtype=np.int32), len(prow))
+            t0 = time.perf_counter()
+            oracle.sink_attention(pbatch, rows=pr, heads=ph, n_threads=cores)
+            dt_p = time.perf_counter() - t0
+            sflops = sample_prefill_flops(pbatch, prow)
+            cpu["prefill"] = {"value": sflops / dt_p / 1e9, "unit": "GFLOP/s", "cores": cores, "kind": "oracle",
+                              "sample": f"every 64th row of gptoss_prefill ({len(prow)} rows x 64 heads), "
+                                        f"{dt_p:.2f} s; scaled: the sample's throughput stands for the whole run",
+                              "scaled_full_run_s": prefill_flops(pbatch) / (sflops / dt_p)}
 
     if rank == 0:
         line = {
@@ -674,13 +747,8 @@ def run_ours(args, world, rank, local):
             "ms_per_step": total_ms / args.steps, "ms_per_step_median": statistics.median(times),
             "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": "gptoss_decode", "batch": batch.batch_size,
-                       "kv_len": "U[1024,8192]", "Hq": 64, "Hkv": 8, "head_dim": 64,
-                       "page_size": 16, "split_kv": True, "sinks": True,
-                       "kv_bytes_per_step": bytes_step, "l2": "flushed before every timed step (256 MB memset, then a 256 MB read: cold L2, no dirty lines)",
-                       "parallelism": f"replicas x{world}", "plan_us": plan_us,
-                       "plan_first_us": plan_first_us,
-                       "decode_units": units},
+            "config": headline_config(batch, world),
+            "plan": {"plan_us": plan_us, "plan_first_us": plan_first_us, "decode_units": units},
             "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
             "clocks": clocks, "cpu_baseline": cpu, "decode_graph": graph, "prefill": prefill, "prefill_ragged": ragged, "kv_cache": kvcache,
             "other_shapes": others,

@@ -63,3 +63,13 @@ def test_traffic_table_is_keyed_to_the_current_sources():
     # DRAM reads of the decode capture stay within 1% of the algorithmic bytes
     d = table["decode_gptoss"]
     assert d["dram_bytes_per_launch"] <= 1.01 * d["algorithmic_bytes_per_launch"]
+
+
+def test_sample_prefill_flops_over_all_rows_equals_total():
+    """The CPU baseline's prefill sample is counted row by row; over every
+    row it must give the whole launch's algorithmic flops."""
+    for batch in (syn.make_batch("cnt", [40, 7, 300], [40, 100, 1000], 4, 2, 64, 16, seed=2),
+                  syn.mixed(0, fill_pool=False)):
+        rows = np.arange(batch.total_rows)
+        prefill = [r for r in rows if batch.qo_lens[np.searchsorted(batch.qo_indptr, r, side="right") - 1] > 1]
+        assert bench.sample_prefill_flops(batch, prefill) == bench.prefill_flops(batch)
