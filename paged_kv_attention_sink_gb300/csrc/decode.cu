@@ -37,7 +37,10 @@ constexpr float kLn2 = 0.6931471805599453f;
 template <int D>
 struct DecodeCfg {
     static constexpr int kWarps = kDecodeWarps;
-    static constexpr int kStages = (D == 64) ? 4 : 3;       // per warp
+    // Stages per warp.  At D = 64 three (48 KB of pipeline, 4 CTAs per SM)
+    // stream faster than four (64 KB, 3 CTAs per SM) with the same bytes in
+    // flight per SM: more CTAs absorb the per-unit start-up and the tail.
+    static constexpr int kStages = 3;
     static constexpr int kSubTile = kBlockTokens * 128;       // 16 rows x 128 B (64 dims)
     static constexpr int kTileBytes = kBlockTokens * D * 2;   // K or V of one block
     static constexpr int kStageBytes = 2 * kTileBytes;

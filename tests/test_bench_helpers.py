@@ -61,8 +61,11 @@ def test_traffic_table_is_keyed_to_the_current_sources():
         # bench reports the entry only while the kernel source is the one captured
         assert (bench.traffic_for(src, key) is not None) == (sha == entry["source_sha256"])
     # DRAM reads of the decode capture stay within 1% of the algorithmic bytes
+    # (every KV byte read once); reads plus writes (partial states, out, lse)
+    # within 2%
     d = table["decode_gptoss"]
-    assert d["dram_bytes_per_launch"] <= 1.01 * d["algorithmic_bytes_per_launch"]
+    assert d["dram_read_bytes_per_launch"] <= 1.01 * d["algorithmic_bytes_per_launch"]
+    assert d["dram_bytes_per_launch"] <= 1.02 * d["algorithmic_bytes_per_launch"]
 
 
 def test_sample_prefill_flops_over_all_rows_equals_total():
