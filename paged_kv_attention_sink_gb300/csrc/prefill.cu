@@ -532,6 +532,16 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
             const int last_key = it.kv_len - 1;
             const int row_limit = a.causal ? min(it.pos0 + r, last_key) : last_key;
             const int first_masked = ((a.causal ? min(it.pos0, last_key) : last_key) + 1) / kPrefillKeys;
+            // The first tile of an item sets the running max.  Later tiles
+            // reuse it and skip the max: P = 2^(s - m) is computed directly,
+            // and only when the tile's row sum exceeds 2^64 (some P could then
+            // be large enough to overflow the sums) is the tile redone: S is
+            // loaded again (it stays in TMEM until the check has passed), the
+            // max raised and O rescaled.  Any max is a valid softmax shift, so
+            // the result does not depend on when it moves.  The redo re-enters
+            // the loop body for the same tile (the S wait returns at once), so
+            // the scores need not stay live past the exponentials.
+            bool redo = false;
             for (int j = 0; j < n; ++j) {
                 const int t = hj + j;
                 if (!wait_all(B.s_full + 8 * i, t & 1)) { ok = false; break; }
@@ -545,20 +555,18 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                     for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(v[e]);
                 }
                 ptx::tc_wait_ld();
-                if (C::kSeparateP) {
-                    // S is in registers: the MMA warp may overwrite it with the next tile.
-                    ptx::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(B.s_free + 8 * i);
-                }
                 if (j >= first_masked) {
                     const int ncol = row_limit - j * kPrefillKeys + 1;
 #pragma unroll
                     for (int c = 0; c < 128; ++c)
                         if (c >= ncol) s[c] = -INFINITY;
                 }
-                // Row max: 16 independent chains of 3-input max, then a tree.
-                auto row_max = [&]() {
+                // At D = 64 the previous PV must be done before O is touched or
+                // P is overwritten (at D = 128 it is: S of tile j waited for it).
+                bool prev_done = !C::kSeparateP || t == 0;
+                if (j == 0 || redo) {
+                    // Raise the running max to cover this tile (row max: 16
+                    // independent chains of 3-input max, then a tree).
                     float mq[16];
 #pragma unroll
                     for (int k = 0; k < 16; ++k)
@@ -567,34 +575,49 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                                           ptx::max3(s[96 + k], s[112 + k], s[112 + k]));
 #pragma unroll
                     for (int k = 0; k < 5; ++k) mq[k] = ptx::max3(mq[k], mq[5 + k], mq[10 + k]);
-                    return ptx::max3(ptx::max3(mq[0], mq[1], mq[2]), ptx::max3(mq[3], mq[4], mq[15]), mq[15]);
-                };
-                // Raise the running max to cover this tile; returns the factor
-                // that rescales the state accumulated so far.
-                auto raise_max = [&]() {
-                    const float m_new = fmaxf(m_use, row_max() * sl2);
+                    const float tmax = ptx::max3(ptx::max3(mq[0], mq[1], mq[2]), ptx::max3(mq[3], mq[4], mq[15]), mq[15]);
+                    const float m_new = fmaxf(m_use, tmax * sl2);
                     const float alpha = m_new > m_use ? ptx::ex2(m_use - m_new) : 1.f;
                     l *= alpha;
                     le *= alpha;
                     m_use = m_new;
-                    return alpha;
-                };
-                // The first tile of an item sets the running max.  Later tiles
-                // reuse it and skip the max: P = 2^(s - m) is computed directly,
-                // and only when the tile's row sum exceeds 2^64 (some P could
-                // then be large enough to overflow the sums) is the max raised,
-                // O rescaled and the tile recomputed.  Any max is a valid
-                // softmax shift, so the result does not depend on when it moves.
-                if (j == 0) raise_max();
-                // At D = 64 the previous PV must be done before O is touched or
-                // P is overwritten (at D = 128 it is: S of tile j waited for it).
-                bool prev_done = !C::kSeparateP || t == 0;
+                    if (redo) {   // rescale what the earlier tiles put in O
+                        if (!prev_done) {
+                            if (!wait_all(B.o_done + 8 * i, (t - 1) & 1)) { ok = false; break; }
+                            prev_done = true;
+                            ptx::tc_fence_after();
+                        }
+#pragma unroll
+                        for (int c = 0; c < D / 32; ++c) {
+                            uint32_t v[32];
+                            ptx::tmem_ld32(t_o + c * 32, v);
+                            ptx::tc_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                            ptx::tmem_st32(t_o + c * 32, v);
+                        }
+                        if constexpr (C::kSplitP) {   // the row-sum columns
+                            uint32_t v[16];
+                            ptx::tmem_ld16(t_o + D, v);
+                            ptx::tc_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                            ptx::tmem_st16(t_o + D, v);
+                        }
+                        ptx::tc_wait_st();
+                    }
+                }
                 uint32_t pk[2][32];
                 float tile_l = 0.f, tile_le = 0.f;
                 const bool take_turns = C::kSplitP && it.n_heads == 2;
-                if (take_turns && !wait_all(my_turn, n_turn & 1)) { ok = false; break; }
-#pragma unroll 1
-                for (int pass = 0;; ++pass) {
+                // The turn is handed over right after the exponentials, before the
+                // overflow check.  A redo runs outside the turn order: the turn
+                // only spaces out the two warps' MUFU use, and each warp must
+                // take exactly one turn per tile, or a warp that redoes tiles
+                // would wait for hand-overs that its partner, tiles ahead,
+                // cannot give before the K and V rings wait for this warp.
+                if (take_turns && !redo && !wait_all(my_turn, n_turn & 1)) { ok = false; break; }
+                {
                     const float neg_m = m_use == -INFINITY ? 0.f : -m_use;
                     const float2 sl2x2 = make_float2(sl2, sl2), negm2 = make_float2(neg_m, neg_m);
                     // Pairs on the FMA pipe: y = sat(s * sl2 / R + 1/2 - m / R).
@@ -622,35 +645,23 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                     const float2 lsum = ptx::add2(ls2[0], ls2[1]), lxsum = ptx::add2(lx2[0], lx2[1]);
                     tile_l = lsum.x + lsum.y;
                     tile_le = lxsum.x + lxsum.y;
-                    if (j == 0 || pass > 0 || !__any_sync(0xffffffffu, tile_le > kSumLimit)) break;
-                    const float alpha = raise_max();
-                    if (!prev_done) {
-                        if (!wait_all(B.o_done + 8 * i, (t - 1) & 1)) { ok = false; break; }
-                        prev_done = true;
-                        ptx::tc_fence_after();
-                    }
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t v[32];
-                        ptx::tmem_ld32(t_o + c * 32, v);
-                        ptx::tc_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                        ptx::tmem_st32(t_o + c * 32, v);
-                    }
-                    if constexpr (C::kSplitP) {   // the row-sum columns
-                        uint32_t v[16];
-                        ptx::tmem_ld16(t_o + D, v);
-                        ptx::tc_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                        ptx::tmem_st16(t_o + D, v);
-                    }
                 }
-                if (take_turns) {
+                if (take_turns && !redo) {
                     __syncwarp();
                     if (lane == 0) ptx::mbar_arrive(other_turn);
                     ++n_turn;
+                }
+                if (j > 0 && !redo && __any_sync(0xffffffffu, tile_le > kSumLimit)) {
+                    redo = true;
+                    --j;
+                    continue;
+                }
+                redo = false;
+                if (C::kSeparateP) {
+                    // S is no longer needed: the MMA warp may overwrite it with the next tile.
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(B.s_free + 8 * i);
                 }
                 if (!ok) break;
                 l += tile_l;

@@ -101,16 +101,36 @@ def _scale_keys(batch, b, lo, hi, factor):
     batch.kv_pool = syn.bf16_bits(k)
 
 
+@pytest.mark.parametrize("head_dim", [64, 128])
 @pytest.mark.parametrize("causal", [True, False])
-def test_prefill_max_jumps_past_sum_limit(causal):
+def test_prefill_max_jumps_mid_item(causal, head_dim):
     """Later key tiles score far above the first tile (by more than 64 in
-    log2 units), so a tile's P row sum passes the limit and the running max
-    is raised mid-item, O rescaled and the tile recomputed -- twice."""
-    batch = syn.make_batch("jump", [700], [700], 4, 1, 64, 16, causal=causal, seed=12)
+    log2 units), so a tile's P row sum passes the limit and the tile is
+    redone: S reloaded from TMEM, the running max raised mid-item and O
+    rescaled -- twice."""
+    batch = syn.make_batch("jump", [700], [700], 4, 1, head_dim, 16, causal=causal, seed=12)
     _scale_keys(batch, 0, 300, 500, 30.0)
     _scale_keys(batch, 0, 500, 700, 80.0)
     out, lse, _ = run_prefill(batch)
-    _check_rows(batch, out, lse, what=f"max jump causal={causal}")
+    _check_rows(batch, out, lse, what=f"max jump causal={causal} D={head_dim}")
+
+
+@pytest.mark.parametrize("head_dim", [64, 128])
+def test_prefill_huge_key_element_in_a_dimension_queries_zero(head_dim):
+    """A key element of 3e4 in a dimension every query has zeroed leaves the
+    scores as they were: the output must not see it."""
+    batch = syn.make_batch("zerodim", [600], [600], 4, 1, head_dim, 16, seed=13)
+    q = syn.bf16_to_float(batch.q)
+    q[..., 5] = 0.0
+    batch.q = syn.bf16_bits(q)
+    k = syn.bf16_to_float(batch.kv_pool)
+    P = batch.page_size
+    for t in (200, 450):
+        page = batch.page_table[batch.kv_indptr[0] + t // P]
+        k[page, 0, :, t % P, 5] = 3.0e4
+    batch.kv_pool = syn.bf16_bits(k)
+    out, lse, _ = run_prefill(batch)
+    _check_rows(batch, out, lse, what=f"huge key element D={head_dim}")
 
 
 def test_gptoss_prefill_full():
