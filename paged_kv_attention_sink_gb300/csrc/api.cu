@@ -62,13 +62,13 @@ bool make_ragged_map(void* map, const void* x, const attn_plan_s* p) {
 // q (or out) [rows][Hq][D] as a 3-D tensor {dim, head, row}: one box is 128
 // rows x 64 dims of one head; rows past the end read as zero (and are not
 // written by a store).
-bool make_q_map(void* map, const void* q, const attn_plan_s* p) {
+bool make_q_map(void* map, const void* q, const attn_plan_s* p, uint32_t box_rows = attn::kPrefillRows) {
     auto fn = encode_fn();
     if (!fn) return false;
     const int64_t rows = p->info.total_qo_rows;
     cuuint64_t dims[3] = {(cuuint64_t)p->D, (cuuint64_t)p->Hq, (cuuint64_t)rows};
     cuuint64_t strides[2] = {(cuuint64_t)p->D * 2, (cuuint64_t)p->Hq * p->D * 2};
-    cuuint32_t box[3] = {64, 1, (cuuint32_t)attn::kPrefillRows};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
     cuuint32_t elem[3] = {1, 1, 1};
     return fn(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
               const_cast<void*>(q), dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -179,7 +179,7 @@ extern "C" attn_status attn_prefill(attn_plan_t plan, const void* q, const void*
         plan->q_map_prefill_ptr = q;
     }
     if (plan->o_map_prefill_ptr != out) {
-        if (!make_q_map(plan->o_map_prefill, out, plan)) return ATTN_ERR_CUDA;
+        if (!make_q_map(plan->o_map_prefill, out, plan, attn::kPrefillOutRows)) return ATTN_ERR_CUDA;
         plan->o_map_prefill_ptr = out;
     }
     return attn::launch_prefill(plan, plan->q_map_prefill, plan->kv_map_prefill, nullptr, plan->o_map_prefill,
@@ -207,7 +207,7 @@ extern "C" attn_status attn_prefill_ragged(attn_plan_t plan, const void* q, cons
         plan->q_map_prefill_ptr = q;
     }
     if (plan->o_map_prefill_ptr != out) {
-        if (!make_q_map(plan->o_map_prefill, out, plan)) return ATTN_ERR_CUDA;
+        if (!make_q_map(plan->o_map_prefill, out, plan, attn::kPrefillOutRows)) return ATTN_ERR_CUDA;
         plan->o_map_prefill_ptr = out;
     }
     return attn::launch_prefill(plan, plan->q_map_prefill, plan->kv_map_prefill, plan->v_map_prefill,

@@ -19,6 +19,7 @@ constexpr int kDecodeMinChunkBlocks = 8;  // never split a sequence finer than 1
 constexpr int kDecodeMaxChunkBlocks = 512;
 constexpr int kDecodeMaxChunkPages = kDecodeMaxChunkBlocks * kBlockTokens / 16 + 2;
 constexpr int kPrefillRows = 128;         // query rows per prefill tile (TMEM lanes)
+constexpr int kPrefillOutRows = 32;       // rows per output TMA store (one softmax warp's stripe)
 constexpr int kPrefillKeys = 128;         // keys per prefill KV tile
 constexpr int kGraphMaxBatch = 4096;      // attn_graph_plan: requests the device planner can order
 
@@ -128,6 +129,6 @@ struct attn_plan_s {
     const void* q_map_prefill_ptr = nullptr;
     alignas(64) unsigned char v_map_prefill[128];   // ragged: K in kv_map_prefill, V here
     const void* v_map_prefill_ptr = nullptr;
-    alignas(64) unsigned char o_map_prefill[128];   // out, laid out like q
+    alignas(64) unsigned char o_map_prefill[128];   // out, laid out like q, 32-row boxes
     const void* o_map_prefill_ptr = nullptr;
 };

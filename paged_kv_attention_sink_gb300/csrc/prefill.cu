@@ -75,7 +75,7 @@ struct PrefillCfg {
     static constexpr bool kSeparateP = (D == 64);
     static constexpr int kQBufs = (D == 64) ? 2 : 1;
     static constexpr int kStagesK = (D == 64) ? 3 : 2;
-    static constexpr int kStagesV = (D == 64) ? 3 : 2;
+    static constexpr int kStagesV = 2;
     static constexpr int kAtom = 128 * 128;              // 128 rows x 64 bf16, swizzled
     static constexpr int kTile = kAtom * (D / 64);       // Q, K or V tile of 128 rows
     static constexpr int kOffQ = 0;
@@ -89,9 +89,12 @@ struct PrefillCfg {
     static constexpr bool kSplitP = (D == 64);
     static constexpr int kON = kSplitP ? D + 16 : D;      // O accumulator columns
     static constexpr int kOffPb = kOffV + kStagesV * kTile;                 // per head 128 rows x 128 B
-    static constexpr int kOffOnes = kOffPb + (kSplitP ? 2 * kAtom : 0);     // 16 key rows x 128 B
+    // D = 64: per head slot, the output tile staged for its TMA store (each
+    // warp's 32-row stripe leaves in its own store).
+    static constexpr int kOffStage = kOffPb + (kSplitP ? 2 * kAtom : 0);
+    static constexpr int kOffOnes = kOffStage + (kSplitP ? 2 * kAtom : 0);  // 16 key rows x 128 B
     static constexpr int kOffBar = kOffOnes + (kSplitP ? 2048 : 0);
-    static constexpr int kNumBars = 2 * kQBufs + 2 * kStagesK + 2 * kStagesV + 8 + 2 + 8 + 4;
+    static constexpr int kNumBars = 2 * kQBufs + 2 * kStagesK + 2 * kStagesV + 8 + 2 + 8;
     static constexpr int kSmem = 1024 + kOffBar + kNumBars * 8 + 16;
     static constexpr uint32_t kTmemCols = 512;
     // TMEM columns of head slot i (every region starts on a multiple of 32).
@@ -116,7 +119,7 @@ struct PrefillArgs {
 
 struct Bars {
     uint32_t q_full, q_empty, k_full, k_empty, v_full, v_empty, s_full, s_free, p_full, o_done,
-        v_aux, drain, turn, o_staged, o_free;
+        v_aux, drain, turn;
 };
 
 // Warp-uniform bounded wait.
@@ -156,8 +159,6 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
     B.v_aux = B.o_done + 16;
     B.drain = B.v_aux + 8;
     B.turn = B.drain + 8;   // [quadrant][head slot]
-    B.o_staged = B.turn + 64;   // [head slot]: the 4 warps' output rows are in shared memory
-    B.o_free = B.o_staged + 16; // [head slot]: the output store has read them
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int item_begin = a.item_off[blockIdx.x], item_end = a.item_off[blockIdx.x + 1];
@@ -186,10 +187,6 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
         ptx::mbar_init(B.v_aux, 1);
         ptx::mbar_init(B.drain, 2);
         for (int k = 0; k < 8; ++k) ptx::mbar_init(B.turn + 8 * k, 1);
-        for (int k = 0; k < 2; ++k) {
-            ptx::mbar_init(B.o_staged + 8 * k, 4);
-            ptx::mbar_init(B.o_free + 8 * k, 1);
-        }
         *abort_flag = 0;
         ptx::prefetch_tmap(&q_map);
         ptx::prefetch_tmap(&kv_map);
@@ -419,6 +416,9 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
             nx_tiles = a.items[item_begin].n_kv_tiles;
             nx_heads = a.items[item_begin].n_heads;
         }
+        // D = 64: an item's last PV waits for its P, so the next item's first
+        // QK^T (which needs only its Q, K and the S buffer) goes ahead of it.
+        bool pre = false;   // this item's first QK^T is already issued
         for (int item = item_begin; ok && item < item_end; ++item, ++n_item) {
             if (*abort_flag) { ok = false; break; }
             const int n = nx_tiles, n_heads = nx_heads;
@@ -427,7 +427,7 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                 nx_heads = a.items[item + 1].n_heads;
             }
             const int qb = n_item % C::kQBufs;
-            if (!wait_all(B.q_full + 8 * qb, (n_item / C::kQBufs) & 1)) { ok = false; break; }
+            if (!pre && !wait_all(B.q_full + 8 * qb, (n_item / C::kQBufs) & 1)) { ok = false; break; }
             if (i >= n_heads) {
                 // This head slot has no work in the item: only keep the
                 // shared stages' arrival counts (after each stage is loaded).
@@ -445,14 +445,23 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
             }
             if (C::kSeparateP) {
                 // QK^T of tile j+1 is issued before PV of tile j.
-                if (!kfull(jg)) { ok = false; break; }
-                if (hj > 0 && !wait_all(B.s_free + 8 * i, (hj - 1) & 1)) { ok = false; break; }
-                qk(qb, jg % C::kStagesK, n == 1);
+                if (!pre) {
+                    if (!kfull(jg)) { ok = false; break; }
+                    if (hj > 0 && !wait_all(B.s_free + 8 * i, (hj - 1) & 1)) { ok = false; break; }
+                    qk(qb, jg % C::kStagesK, n == 1);
+                }
+                pre = false;
                 for (int j = 0; j < n; ++j) {
                     const int t = jg + j;
                     if (j + 1 < n) {
                         if (!kfull(t + 1) || !wait_all(B.s_free + 8 * i, (hj + j) & 1)) { ok = false; break; }
                         qk(qb, (t + 1) % C::kStagesK, j + 2 == n);
+                    } else if (item + 1 < item_end && i < nx_heads) {
+                        const int qb2 = (n_item + 1) % C::kQBufs;
+                        if (!wait_all(B.q_full + 8 * qb2, ((n_item + 1) / C::kQBufs) & 1) || !kfull(t + 1) ||
+                            !wait_all(B.s_free + 8 * i, (hj + j) & 1)) { ok = false; break; }
+                        qk(qb2, (t + 1) % C::kStagesK, nx_tiles == 1);
+                        pre = true;
                     }
                     if (!vfull(t) || !wait_all(B.p_full + 8 * i, (hj + j) & 1)) { ok = false; break; }
                     pv(t % C::kStagesV, j == 0);
@@ -499,15 +508,87 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
         // waits and stores.  Head slot 0 goes first.
         const uint32_t my_turn = B.turn + 8 * (quad * 2 + i), other_turn = B.turn + 8 * (quad * 2 + (i ^ 1));
         int n_turn = 0;
-        // D = 64: a full 128-row tile's output leaves through the P buffer of
-        // this head slot and one TMA store (rows one thread apart are 8 KB
-        // apart in `out`, so per-thread stores would touch 32 lines per
-        // instruction).  The buffer is reused for the next item's P only
-        // after the store has read it.
-        const uint32_t pb_base = sbase + C::kOffPb + i * C::kAtom;
-        const bool o_leader = (tid & 127) == 0;   // thread 0 of this head slot's warpgroup
-        bool o_pending = false;
-        int n_ostore = 0;
+        // Deferred epilogue: an item's O is read from TMEM, normalised and
+        // stored during this head slot's next item's first tile, after its
+        // exponentials -- the item's last PV has finished by then (the MMA
+        // warp issues the next item's first QK^T ahead of it), and the work
+        // overlaps the other head slot's exponentials instead of stalling
+        // both.  PV of that tile overwrites O, so it runs before P is stored.
+        // D = 64: a warp's 32 full rows leave through the staging tile and
+        // one TMA store (rows one thread apart are 8 KB apart in `out`, so
+        // per-thread stores would touch 32 lines per instruction); the stripe
+        // is reused one item later, after this warp's store has read it.
+        const uint32_t st_stripe = sbase + C::kOffStage + i * C::kAtom + quad * 4096;
+        const uint32_t st_row = st_stripe + (lane >> 3) * 1024 + (lane & 7) * 128;
+        // The pending item is kept as its index, its lse and the sink's part
+        // of its row sum (three registers across the next item's tile).
+        bool epi = false;
+        int e_item = 0;
+        float e_l = 0.f, e_lse = 0.f;
+        auto epilogue = [&]() -> bool {
+            if (!wait_all(B.o_done + 8 * i, (hj - 1) & 1)) return false;   // its last PV
+            const PrefillItem ei = a.items[e_item];
+            const int e_row0 = ei.q_row0, e_head = ei.head0 + i, e_rows = ei.n_rows;
+            ptx::tc_fence_after();
+            float lt = e_l;
+            if constexpr (C::kSplitP) {   // the keys' part of the row sum, next to O
+                uint32_t v[16];
+                ptx::tmem_ld16(t_o + D, v);
+                ptx::tc_wait_ld();
+                lt += __uint_as_float(v[0]);
+            }
+            const float inv = lt > 0.f ? 1.f / lt : 0.f;
+            if (C::kSplitP && quad * 32 + 32 <= e_rows) {
+                if (lane == 0) ptx::bulk_wait_read_all();   // the stripe's previous store has read it
+                __syncwarp();
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t v[32];
+                    ptx::tmem_ld32(t_o + c * 32, v);
+                    ptx::tc_wait_ld();
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int e = 8 * q;
+                        ptx::st_shared_v4(
+                            st_row + (((c * 4 + q) ^ (lane & 7)) << 4),
+                            ptx::pack_bf16x2(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv),
+                            ptx::pack_bf16x2(__uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv),
+                            ptx::pack_bf16x2(__uint_as_float(v[e + 4]) * inv, __uint_as_float(v[e + 5]) * inv),
+                            ptx::pack_bf16x2(__uint_as_float(v[e + 6]) * inv, __uint_as_float(v[e + 7]) * inv));
+                    }
+                }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    ptx::tma_store_3d(&o_map, st_stripe, 0, e_head, e_row0 + quad * 32);
+                    ptx::bulk_commit_group();
+                }
+            } else {
+                // Rows of a ragged last tile (a box would overwrite the next
+                // request's rows) and D = 128: per-thread stores.
+                const bool store = r < e_rows;
+                __nv_bfloat16* orow = a.out + ((size_t)(e_row0 + r) * a.Hq + e_head) * D;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t v[32];
+                    ptx::tmem_ld32(t_o + c * 32, v);
+                    ptx::tc_wait_ld();
+                    if (store) {
+#pragma unroll
+                        for (int e = 0; e < 32; e += 8) {
+                            uint4 w;
+                            w.x = ptx::pack_bf16x2(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv);
+                            w.y = ptx::pack_bf16x2(__uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv);
+                            w.z = ptx::pack_bf16x2(__uint_as_float(v[e + 4]) * inv, __uint_as_float(v[e + 5]) * inv);
+                            w.w = ptx::pack_bf16x2(__uint_as_float(v[e + 6]) * inv, __uint_as_float(v[e + 7]) * inv);
+                            *reinterpret_cast<uint4*>(orow + c * 32 + e) = w;
+                        }
+                    }
+                }
+            }
+            if (r < e_rows && a.lse) a.lse[(size_t)(e_row0 + r) * a.Hq + e_head] = e_lse;
+            return true;
+        };
         if (i == 1 && lane == 0) ptx::mbar_arrive(other_turn);
         // Item descriptors and sinks are read from L1: the sinks' lines are
         // prefetched here, each next descriptor after the current item's last
@@ -664,20 +745,15 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                     if (lane == 0) ptx::mbar_arrive(B.s_free + 8 * i);
                 }
                 if (!ok) break;
+                if (epi) {   // the previous item's output (only ever pending at j == 0)
+                    if (!epilogue()) { ok = false; break; }
+                    epi = false;
+                }
                 l += tile_l;
                 le += tile_le;
                 if (!prev_done) {
                     if (!wait_all(B.o_done + 8 * i, (t - 1) & 1)) { ok = false; break; }
                     ptx::tc_fence_after();
-                }
-                if (C::kSplitP && o_pending) {
-                    // The previous item's output store must have read the buffer.
-                    if (o_leader) {
-                        ptx::bulk_wait_read_all();
-                        ptx::mbar_arrive(B.o_free + 8 * i);
-                    }
-                    if (!wait_all(B.o_free + 8 * i, (n_ostore - 1) & 1)) { ok = false; break; }
-                    o_pending = false;
                 }
                 ptx::tmem_st32(t_p, pk[0]);
                 if constexpr (C::kSplitP) {
@@ -697,76 +773,15 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
             if (!ok) break;
             if (item + 1 < item_end && lane < 2)   // a descriptor may straddle two lines
                 ptx::prefetch_l1(reinterpret_cast<const char*>(a.items + item + 1) + lane * (sizeof(PrefillItem) - 1));
-            // Epilogue: O of this item is complete once the last PV is done.
-            if (!wait_all(B.o_done + 8 * i, (hj + n - 1) & 1)) { ok = false; break; }
-            ptx::tc_fence_after();
+            epi = true;
+            e_item = item;
+            e_l = l;
+            e_lse = le > 0.f ? (m_use + log2f(le)) * kLn2 : -INFINITY;
             hj += n;
-            if constexpr (C::kSplitP) {
-                uint32_t v[16];
-                ptx::tmem_ld16(t_o + D, v);
-                ptx::tc_wait_ld();
-                l += __uint_as_float(v[0]);
-            }
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            const bool store = r < it.n_rows;
-            __nv_bfloat16* orow = a.out + ((size_t)(it.q_row0 + r) * a.Hq + head) * D;
-            if (C::kSplitP && it.n_rows == kPrefillRows) {
-                // Row r of O, normalised and rounded, into the P buffer with the
-                // out tensor map's 128-byte swizzle; then one TMA store.
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t v[32];
-                    ptx::tmem_ld32(t_o + c * 32, v);
-                    ptx::tc_wait_ld();
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int e = 8 * q;
-                        ptx::st_shared_v4(
-                            pb_row + (((c * 4 + q) ^ (r & 7)) << 4),
-                            ptx::pack_bf16x2(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv),
-                            ptx::pack_bf16x2(__uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv),
-                            ptx::pack_bf16x2(__uint_as_float(v[e + 4]) * inv, __uint_as_float(v[e + 5]) * inv),
-                            ptx::pack_bf16x2(__uint_as_float(v[e + 6]) * inv, __uint_as_float(v[e + 7]) * inv));
-                    }
-                }
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(B.o_staged + 8 * i);
-                if ((tid & 127) < 32) {   // the leader's warp waits for all four
-                    if (!wait_all(B.o_staged + 8 * i, n_ostore & 1)) {
-                        ok = false;
-                    } else if (o_leader) {
-                        ptx::tma_store_3d(&o_map, pb_base, 0, head, it.q_row0);
-                        ptx::bulk_commit_group();
-                    }
-                }
-                o_pending = true;
-                ++n_ostore;
-            } else {
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t v[32];
-                ptx::tmem_ld32(t_o + c * 32, v);
-                ptx::tc_wait_ld();
-                if (store) {
-#pragma unroll
-                    for (int e = 0; e < 32; e += 8) {
-                        uint4 w;
-                        w.x = ptx::pack_bf16x2(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv);
-                        w.y = ptx::pack_bf16x2(__uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv);
-                        w.z = ptx::pack_bf16x2(__uint_as_float(v[e + 4]) * inv, __uint_as_float(v[e + 5]) * inv);
-                        w.w = ptx::pack_bf16x2(__uint_as_float(v[e + 6]) * inv, __uint_as_float(v[e + 7]) * inv);
-                        *reinterpret_cast<uint4*>(orow + c * 32 + e) = w;
-                    }
-                }
-            }
-            }
-            if (store && a.lse)
-                a.lse[(size_t)(it.q_row0 + r) * a.Hq + head] =
-                    le > 0.f ? (m_use + log2f(le)) * kLn2 : -INFINITY;
         }
+        if (ok && epi) ok = epilogue();
         if (!ok) fail(ATTN_DEVICE_ERR_TIMEOUT);
-        if (o_leader) ptx::bulk_wait_all();   // output stores complete before the CTA exits
+        if (lane == 0) ptx::bulk_wait_all();   // output stores complete before the CTA exits
     }
 
     // Tear-down: each MMA thread's last commit arrives on `drain` once every
