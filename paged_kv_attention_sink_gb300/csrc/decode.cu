@@ -118,6 +118,11 @@ decode_sink_attn_kernel(const __grid_constant__ CUtensorMap kv_map, const Decode
     const uint64_t policy = ptx::policy_evict_first();
     int gbase = 0;   // stage uses of this warp's ring so far (across units)
 
+    // The persistent grid is launched as a programmatic dependent of the
+    // device planner: its CTAs start (and do the set-up above) while the
+    // planner runs, and wait here until the planner's unit list is complete
+    // and visible.  Without such a launch the wait returns at once.
+    if constexpr (kPersistent) asm volatile("griddepcontrol.wait;" ::: "memory");
     const int n_units = kPersistent ? *a.n_units_dev : 0;
     while (true) {
     int unit = blockIdx.x;
@@ -537,6 +542,9 @@ __global__ void __launch_bounds__(kPlanThreads) decode_graph_plan_kernel(const G
     int* s_poff = s_uoff + p.max_batch;
     int* s_goff = s_poff + p.max_batch;
 
+    // Let the persistent decode grid launch now: its CTAs set up and then wait
+    // (griddepcontrol.wait) for this grid to finish.
+    asm volatile("griddepcontrol.launch_dependents;");
     int B = *p.batch;
     if (B < 0 || B > p.max_batch) {
         if (tid == 0) atomicOr(p.err, ATTN_DEVICE_ERR_PLAN);
@@ -713,6 +721,21 @@ cudaError_t launch(const CUtensorMap& map, const DecodeArgs& args, int grid, cud
         return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     });
     if (e != cudaSuccess) return e;
+    if constexpr (kPersistent) {
+        // A programmatic dependent of the device planner launched just before
+        // on the same stream (see griddepcontrol in both kernels).
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(C::kWarps * 32);
+        cfg.dynamicSmemBytes = C::kSmem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kernel, map, args);
+    }
     kernel<<<grid, C::kWarps * 32, C::kSmem, stream>>>(map, args);
     return cudaGetLastError();
 }
