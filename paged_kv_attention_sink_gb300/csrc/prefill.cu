@@ -776,7 +776,9 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
             epi = true;
             e_item = item;
             e_l = l;
-            e_lse = le > 0.f ? (m_use + log2f(le)) * kLn2 : -INFINITY;
+            // le >= 1 here (the term that set the running max contributes 1), so
+            // the MUFU's approximate lg2 is within 2^-22 of log2(le).
+            e_lse = le > 0.f ? (m_use + __log2f(le)) * kLn2 : -INFINITY;
             hj += n;
         }
         if (ok && epi) ok = epilogue();
