@@ -53,6 +53,191 @@ struct DecodeCfg {
     static_assert(kBlockTokens * kRowStride * 4 <= kStages * kStageBytes, "combine fits");
 };
 
+struct GraphPlanArgs {
+    const int32_t* kv_indptr;       // [batch + 1] page CSR
+    const int32_t* last_page_len;   // [batch]
+    const int32_t* batch;           // device scalar
+    int32_t max_batch, Hq, Hkv, P, n_slices;
+    int64_t target_units;
+    int64_t cap_blocks;             // 16-token blocks the plan's capacity allows
+    int32_t cap_units, cap_groups;
+    DecodeUnit* units;
+    int32_t* n_units;
+    int32_t* queue;                 // [2], then the split-merge counters
+    int32_t* err;
+};
+
+// Token range [c * nblk / nc, (c + 1) * nblk / nc) blocks, in 32-bit
+// arithmetic when the product fits (the common case).
+__device__ __forceinline__ int64_t chunk_block(int c, int64_t nblk, int nc) {
+    const uint64_t prod = (uint64_t)c * (uint64_t)nblk;
+    return prod < 0xFFFFFFFFull ? (int64_t)((uint32_t)prod / (uint32_t)nc) : (int64_t)(prod / (uint64_t)nc);
+}
+
+// Graph plans of up to kInPlanMaxBatch requests are planned inside the
+// persistent decode grid instead of by decode_graph_plan_kernel: every CTA
+// builds the same tables (one request per thread) and derives each unit it
+// takes from them, so no planner launch runs before the decode.  The tables
+// are indexed by sorted position (longest unit first, ties by request).
+constexpr int kInPlanMaxBatch = kDecodeWarps * 32;
+struct InPlan {
+    int32_t uoff[kInPlanMaxBatch + 1];   // first unit of each sorted request; [n] = unit count
+    int32_t nc[kInPlanMaxBatch];         // chunks
+    int32_t req[kInPlanMaxBatch];        // request index (query row)
+    int32_t base[kInPlanMaxBatch];       // kv_indptr[req]
+    int32_t kv[kInPlanMaxBatch];         // kv_len
+    int32_t poff[kInPlanMaxBatch];       // first partial slot
+    int32_t goff[kInPlanMaxBatch];       // first split group
+    int32_t ulen[kInPlanMaxBatch];       // unit length by request (for the ranking)
+    int32_t scan[3][kDecodeWarps];
+    long long blocks[kDecodeWarps];
+    int32_t n, n_groups;
+};
+
+// Builds the tables (all threads of the CTA take part; one request per
+// thread) and returns the unit count, 0 when the batch is refused.  The rule
+// is decode_graph_plan_kernel's: kv lengths from the page CSR, chunk = total
+// blocks / target units clamped to 8..512 blocks, each request's chunk count
+// and unit length, longest first.  `report`: this CTA sets the error word.
+__device__ int plan_in_cta(const GraphPlanArgs& p, InPlan& s, bool report) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int B = *p.batch;
+    bool bad = false;
+    if (B < 0 || B > p.max_batch) {
+        bad = true;
+        B = B < 0 ? 0 : p.max_batch;
+    }
+    int kv = -1, base = 0;
+    if (tid < B) {
+        base = p.kv_indptr[tid];
+        const int64_t np = (int64_t)p.kv_indptr[tid + 1] - base;
+        const int32_t lpl = p.last_page_len[tid];
+        int64_t len = -1;
+        if (np >= 1 && lpl >= 1 && lpl <= p.P) len = (np - 1) * p.P + lpl;
+        if (len < 0 || len > INT32_MAX) {
+            bad = true;
+            len = -1;
+        }
+        kv = (int)len;
+    }
+    long long blocks = kv > 0 ? (kv + kBlockTokens - 1) / kBlockTokens : 0;
+    for (int o = 16; o > 0; o >>= 1) blocks += __shfl_xor_sync(0xffffffffu, blocks, o);
+    if (lane == 0) s.blocks[warp] = blocks;
+    bad = __syncthreads_or(bad);
+    long long total_blocks = 0;
+#pragma unroll
+    for (int w = 0; w < kDecodeWarps; ++w) total_blocks += s.blocks[w];
+    if (total_blocks > p.cap_blocks) {
+        if (report && tid == 0) atomicOr(p.err, ATTN_DEVICE_ERR_PLAN);
+        if (tid == 0) s.n_groups = 0;
+        __syncthreads();
+        return 0;
+    }
+    total_blocks *= (long long)p.Hkv * p.n_slices;
+    const uint32_t chunk = (uint32_t)min((long long)kDecodeMaxChunkBlocks,
+                                         max((long long)kDecodeMinChunkBlocks,
+                                             (total_blocks + p.target_units - 1) / p.target_units));
+    int nc = 0, ulen = 0;
+    if (kv >= 0) {
+        const uint32_t nblk = ((uint32_t)kv + kBlockTokens - 1) / kBlockTokens;
+        const uint32_t n = max(max(1u, (nblk + chunk / 2) / chunk), (nblk + kDecodeMaxChunkBlocks - 1) / kDecodeMaxChunkBlocks);
+        nc = (int)n;
+        ulen = (int)((nblk + n - 1) / n);
+    }
+    if (tid < B) s.ulen[tid] = ulen;
+    __syncthreads();
+    // Sorted position: longer units first, ties by request index (the same
+    // order in every CTA).
+    if (tid < B) {
+        int rank = 0;
+        for (int b = 0; b < B; ++b) {
+            const int u = s.ulen[b];
+            rank += (u > ulen) || (u == ulen && b < tid);
+        }
+        s.req[rank] = tid;
+        s.nc[rank] = nc;
+        s.base[rank] = base;
+        s.kv[rank] = kv;
+    }
+    __syncthreads();
+    // Exclusive scans over sorted positions: units, partial slots, groups.
+    const int per_req = p.Hkv * p.n_slices;
+    int v[3] = {0, 0, 0};
+    if (tid < B) {
+        const int n = s.nc[tid];
+        v[0] = n * per_req;
+        if (n > 1) {
+            v[1] = n * per_req;
+            v[2] = per_req;
+        }
+    }
+    int inc[3] = {v[0], v[1], v[2]};
+#pragma unroll
+    for (int k = 0; k < 3; ++k)
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, inc[k], o);
+            if (lane >= o) inc[k] += n;
+        }
+    if (lane == 31)
+#pragma unroll
+        for (int k = 0; k < 3; ++k) s.scan[k][warp] = inc[k];
+    __syncthreads();
+    int tot[3], pre[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        tot[k] = pre[k] = 0;
+#pragma unroll
+        for (int w = 0; w < kDecodeWarps; ++w) {
+            tot[k] += s.scan[k][w];
+            if (w < warp) pre[k] += s.scan[k][w];
+        }
+    }
+    if (tid < B) {
+        s.uoff[tid] = pre[0] + inc[0] - v[0];
+        s.poff[tid] = pre[1] + inc[1] - v[1];
+        s.goff[tid] = pre[2] + inc[2] - v[2];
+    }
+    const bool over = tot[0] > p.cap_units || tot[1] > p.cap_units || tot[2] > p.cap_groups;
+    if (tid == 0) {
+        s.uoff[B] = tot[0];
+        s.n = B;
+        s.n_groups = over ? 0 : tot[2];
+        if (report && (bad || over)) atomicOr(p.err, ATTN_DEVICE_ERR_PLAN);
+    }
+    __syncthreads();
+    return over ? 0 : tot[0];
+}
+
+// Unit `u` of the in-grid plan (the fields decode_graph_plan_kernel writes).
+__device__ DecodeUnit unit_of(const InPlan& s, int u, const GraphPlanArgs& p) {
+    int lo = 0, hi = s.n - 1;   // last sorted position whose first unit is <= u
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s.uoff[mid] <= u) lo = mid;
+        else hi = mid - 1;
+    }
+    const int k = u - s.uoff[lo], nc = s.nc[lo];
+    const int gs = k / nc, c = k - gs * nc;
+    const int g = gs / p.n_slices, sl = gs - g * p.n_slices;
+    const int G = p.Hq / p.Hkv;
+    const int64_t kv = s.kv[lo];
+    const int64_t nblk = (kv + kBlockTokens - 1) / kBlockTokens;
+    DecodeUnit d;
+    d.q_row = s.req[lo];
+    d.page_base = s.base[lo];
+    d.kv_head = g;
+    d.head0 = g * G + sl * kMaxSliceHeads;
+    d.n_heads = min(kMaxSliceHeads, G - sl * kMaxSliceHeads);
+    d.tok_begin = (int)(chunk_block(c, nblk, nc) * kBlockTokens);
+    d.tok_end = (int)min(kv, chunk_block(c + 1, nblk, nc) * kBlockTokens);
+    d.chunk = c;
+    d.n_chunks = nc;
+    d.group = nc > 1 ? s.goff[lo] + gs : -1;
+    d.partial0 = nc > 1 ? s.poff[lo] + gs * nc : 0;
+    d.reserved = 0;
+    return d;
+}
+
 struct DecodeArgs {
     const DecodeUnit* units;
     const int32_t* page_table;
@@ -68,6 +253,8 @@ struct DecodeArgs {
     int32_t* err;
     int32_t Hq, Hkv, P, num_pages;
     float scale_log2;   // sm_scale * log2(e)
+    int32_t in_plan;    // persistent launches: plan inside the grid from `gp`
+    GraphPlanArgs gp;
 };
 
 __device__ __forceinline__ uint32_t ld_b32(const __nv_bfloat16* p) {
@@ -104,6 +291,7 @@ decode_sink_attn_kernel(const __grid_constant__ CUtensorMap kv_map, const Decode
     const int P = a.P;
     volatile int* unit_s = flag_s + 1;   // unit handed to this CTA
     volatile int* abort_s = flag_s + 2;
+    volatile int* last_s = flag_s + 3;   // persistent: this CTA finished last
 
     if (lane == 0)
         for (int s = 0; s < C::kStages; ++s) ptx::mbar_init(ptx::smem_u32(&bars[warp * C::kStages + s]), 1);
@@ -123,7 +311,22 @@ decode_sink_attn_kernel(const __grid_constant__ CUtensorMap kv_map, const Decode
     // planner runs, and wait here until the planner's unit list is complete
     // and visible.  Without such a launch the wait returns at once.
     if constexpr (kPersistent) asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int n_units = kPersistent ? *a.n_units_dev : 0;
+    // In-grid plan: its tables sit past the decode's own shared memory.
+    InPlan& ip = *reinterpret_cast<InPlan*>(smem + C::kSmem - 1024);
+    int n_units = 0;
+    if constexpr (kPersistent) {
+        if (a.in_plan) {
+            n_units = plan_in_cta(a.gp, ip, blockIdx.x == 0);
+            if (blockIdx.x == 0) {
+                // The unit list and its count, for inspection (attn_graph_plan_read_units);
+                // no CTA reads them back.
+                for (int u = tid; u < n_units; u += blockDim.x) a.gp.units[u] = unit_of(ip, u, a.gp);
+                if (tid == 0) *a.gp.n_units = n_units;
+            }
+        } else {
+            n_units = *a.n_units_dev;
+        }
+    }
     while (true) {
     int unit = blockIdx.x;
     if constexpr (kPersistent) {
@@ -132,7 +335,7 @@ decode_sink_attn_kernel(const __grid_constant__ CUtensorMap kv_map, const Decode
         unit = *unit_s;
         if (unit >= n_units || *abort_s) break;
     }
-    const DecodeUnit u = a.units[unit];
+    const DecodeUnit u = (kPersistent && a.in_plan) ? unit_of(ip, unit, a.gp) : a.units[unit];
     const int first_page = u.tok_begin / P;
     const int n_pages = (u.tok_end - 1) / P - first_page + 1;
     for (int i = tid; i < n_pages; i += blockDim.x)
@@ -447,12 +650,23 @@ decode_sink_attn_kernel(const __grid_constant__ CUtensorMap kv_map, const Decode
     __syncthreads();   // shared memory is reused by the next unit
     }
 
-    // The last CTA to finish resets the queue for the next launch.
-    if (kPersistent && tid == 0) {
-        __threadfence();
-        if (atomicAdd(&a.queue[1], 1) == (int)gridDim.x - 1) {
-            atomicExch(&a.queue[0], 0);
-            atomicExch(&a.queue[1], 0);
+    // The last CTA to finish resets the queue for the next launch (and, with
+    // the in-grid plan, clears this launch's split counters: after a launch
+    // that ran to the end they are zero already, after one that gave up early
+    // they may not be).
+    if constexpr (kPersistent) {
+        if (tid == 0) {
+            __threadfence();
+            *last_s = atomicAdd(&a.queue[1], 1) == (int)gridDim.x - 1;
+        }
+        __syncthreads();
+        if (*last_s) {
+            if (a.in_plan)
+                for (int g = tid; g < ip.n_groups; g += blockDim.x) a.counters[g] = 0;
+            if (tid == 0) {
+                atomicExch(&a.queue[0], 0);
+                atomicExch(&a.queue[1], 0);
+            }
         }
     }
 }
@@ -466,19 +680,6 @@ decode_sink_attn_kernel(const __grid_constant__ CUtensorMap kv_map, const Decode
 // range of sorted positions while it scans the unit counts.
 constexpr int kPlanThreads = 1024;
 
-struct GraphPlanArgs {
-    const int32_t* kv_indptr;       // [batch + 1] page CSR
-    const int32_t* last_page_len;   // [batch]
-    const int32_t* batch;           // device scalar
-    int32_t max_batch, Hq, Hkv, P, n_slices;
-    int64_t target_units;
-    int64_t cap_blocks;             // 16-token blocks the plan's capacity allows
-    int32_t cap_units, cap_groups;
-    DecodeUnit* units;
-    int32_t* n_units;
-    int32_t* queue;                 // [2], then the split-merge counters
-    int32_t* err;
-};
 
 // Exclusive block-wide scan of three counters (kPlanThreads threads).
 __device__ void block_scan3(int (&v)[3], int (&total)[3], int* sh /* [3][32] */) {
@@ -520,12 +721,6 @@ inline size_t plan_smem_bytes(int max_batch) { return (size_t)max_batch * 7 * si
 constexpr int kPlanPerThread = (kGraphMaxBatch + kPlanThreads - 1) / kPlanThreads;
 static_assert(kPlanPerThread * kPlanThreads >= kGraphMaxBatch, "planner request ownership");
 
-// Token range [c * nblk / nc, (c + 1) * nblk / nc) blocks, in 32-bit
-// arithmetic when the product fits (the common case).
-__device__ __forceinline__ int64_t chunk_block(int c, int64_t nblk, int nc) {
-    const uint64_t prod = (uint64_t)c * (uint64_t)nblk;
-    return prod < 0xFFFFFFFFull ? (int64_t)((uint32_t)prod / (uint32_t)nc) : (int64_t)(prod / (uint64_t)nc);
-}
 
 __global__ void __launch_bounds__(kPlanThreads) decode_graph_plan_kernel(const GraphPlanArgs p) {
     extern __shared__ int plan_smem[];
@@ -716,24 +911,26 @@ template <int D, bool kTwoRows, bool kPersistent>
 cudaError_t launch(const CUtensorMap& map, const DecodeArgs& args, int grid, cudaStream_t stream) {
     using C = DecodeCfg<D>;
     auto kernel = decode_sink_attn_kernel<D, kTwoRows, kPersistent>;
+    // The persistent form also holds the in-grid plan's tables.
+    constexpr int smem = C::kSmem + (kPersistent ? (int)sizeof(InPlan) : 0);
     static std::atomic<bool> configured[kMaxDevices];
     cudaError_t e = once_per_device(configured, [&] {
-        return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+        return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     });
     if (e != cudaSuccess) return e;
     if constexpr (kPersistent) {
-        // A programmatic dependent of the device planner launched just before
-        // on the same stream (see griddepcontrol in both kernels).
+        // Behind the device planner: a programmatic dependent of it (see
+        // griddepcontrol in both kernels).
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(grid);
         cfg.blockDim = dim3(C::kWarps * 32);
-        cfg.dynamicSmemBytes = C::kSmem;
+        cfg.dynamicSmemBytes = smem;
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = args.in_plan ? 0 : 1;
         return cudaLaunchKernelEx(&cfg, kernel, map, args);
     }
     kernel<<<grid, C::kWarps * 32, C::kSmem, stream>>>(map, args);
@@ -776,13 +973,21 @@ DecodeArgs make_args(const attn_plan_s* plan, unsigned char* base, const void* q
     a.P = plan->P;
     a.num_pages = plan->num_pages;
     a.scale_log2 = plan->sm_scale * kLog2e;
+    a.in_plan = 0;
+    a.gp = GraphPlanArgs{};
     return a;
 }
 
 }  // namespace
 
+constexpr int kSmemPerSm = 233472;   // 228 KB; 1 KB of it is reserved per CTA
+// The persistent form's in-grid plan tables must not cost a CTA per SM.
+static_assert(kSmemPerSm / (DecodeCfg<64>::kSmem + (int)sizeof(InPlan) + 1024) ==
+                  kSmemPerSm / (DecodeCfg<64>::kSmem + 1024), "in-grid plan and CTAs per SM (D = 64)");
+static_assert(kSmemPerSm / (DecodeCfg<128>::kSmem + (int)sizeof(InPlan) + 1024) ==
+                  kSmemPerSm / (DecodeCfg<128>::kSmem + 1024), "in-grid plan and CTAs per SM (D = 128)");
+
 int decode_ctas_per_sm(int head_dim) {
-    constexpr int kSmemPerSm = 233472;   // 228 KB; 1 KB of it is reserved per CTA
     const int per_cta = (head_dim == 64 ? DecodeCfg<64>::kSmem : DecodeCfg<128>::kSmem) + 1024;
     return kSmemPerSm / per_cta;
 }
@@ -822,6 +1027,17 @@ attn_status launch_decode_graph(attn_plan_s* plan, const int32_t* kv_indptr, con
     gp.n_units = reinterpret_cast<int32_t*>(plan->ws + plan->layout.n_units);
     gp.queue = reinterpret_cast<int32_t*>(plan->ws + plan->layout.counters);
     gp.err = reinterpret_cast<int32_t*>(plan->ws + plan->layout.err);
+    DecodeArgs a = make_args(plan, plan->ws, q, sinks, out, lse);
+    a.queue = gp.queue;
+    a.counters = gp.queue + 2;
+    a.n_units_dev = gp.n_units;
+    const int grid = plan->num_sms * decode_ctas_per_sm(plan->D);
+    if (plan->batch <= kInPlanMaxBatch) {
+        // Small plans: every CTA of the persistent grid plans for itself.
+        a.in_plan = 1;
+        a.gp = gp;
+        return dispatch<true>(plan, *static_cast<const CUtensorMap*>(kv_map), a, grid, stream);
+    }
     // The shared-memory limit is raised once per device to what the largest
     // graph plan needs; each launch asks only for its own plan's share.
     static std::atomic<bool> configured[kMaxDevices];
@@ -832,11 +1048,6 @@ attn_status launch_decode_graph(attn_plan_s* plan, const int32_t* kv_indptr, con
         return ATTN_ERR_CUDA;
     decode_graph_plan_kernel<<<1, kPlanThreads, plan_smem_bytes(plan->batch), stream>>>(gp);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
-    DecodeArgs a = make_args(plan, plan->ws, q, sinks, out, lse);
-    a.queue = gp.queue;
-    a.counters = gp.queue + 2;
-    a.n_units_dev = gp.n_units;
-    const int grid = plan->num_sms * decode_ctas_per_sm(plan->D);
     return dispatch<true>(plan, *static_cast<const CUtensorMap*>(kv_map), a, grid, stream);
 }
 

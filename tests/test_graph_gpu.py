@@ -99,6 +99,29 @@ def test_device_plan_equals_host_plan(which):
     assert plan.device_error() == 0
 
 
+def test_in_grid_plan_equals_planner_kernel_plan():
+    """Plans of up to 128 requests are built inside the persistent decode grid
+    (every CTA plans for itself), larger ones by the planner kernel: the same
+    batch under a 128-request and a 129-request plan gives the same units and
+    the same output, bit for bit."""
+    kv = np.random.default_rng(16).integers(1, 5000, size=100).tolist()
+    b = syn.make_batch("r100", [1] * 100, kv, 64, 8, 64, 16, seed=16)
+    res = []
+    for max_batch in (128, 129):
+        buf = Buffers(max_batch, 64, 8, 64, 16, b.num_pages, len(b.page_table))
+        buf.load(b)
+        plan = _graph_plan(buf, max_batch, b)
+        _decode(plan, buf)
+        torch.cuda.synchronize()
+        assert plan.device_error() == 0
+        key = lambda u: tuple(int(x) for x in u[:9])
+        res.append((sorted(map(key, plan.device_units())), buf.out[:b.batch_size].clone(), buf.lse[:b.batch_size].clone()))
+    assert res[0][0] == res[1][0]
+    assert torch.equal(res[0][1].view(torch.int16), res[1][1].view(torch.int16))
+    assert torch.equal(res[0][2], res[1][2])
+    _check(b, buf, what="graph decode, 100 requests")
+
+
 @pytest.mark.parametrize("which", ["gptoss", "tiny", "long"])
 def test_graph_decode_matches_oracle(which):
     if which == "gptoss":
