@@ -21,22 +21,25 @@
 //  * warps 1 and 2: tcgen05.mma issuers, one warp per head slot (neither
 //    head's MMAs queue behind the other's softmax), one elected lane issuing.
 //    S_h = Q_h K^T (both operands K-major in shared memory); O_h += P_h V with
-//    V an MN-major shared-memory operand.  At D = 64, P keys 0..63 come from
-//    their own TMEM columns and keys 64..127 from shared memory, and V is
+//    V an MN-major shared-memory operand.  At D = 64, P keys 0..95 come from
+//    their own TMEM columns and keys 96..127 from shared memory, and V is
 //    extended by a ones column so the same MMA accumulates the row sum of the
-//    rounded P; S_h of tile j+1 is computed while the softmax of tile j runs.
-//    At D = 128, P is read from tensor memory where S was.
+//    rounded P; S_h of tile j+1 is computed while the softmax of tile j runs,
+//    and an item's first QK^T goes ahead of the previous item's last PV.  At
+//    D = 128, P is read from tensor memory where S was.
 //  * warps 4-7 / 8-11: softmax of head 0 / head 1, one thread per query row
 //    (= TMEM lane).  Causal / length mask on diagonal and ragged tiles only;
 //    the row max is taken on an item's first tile only; later tiles keep it
-//    unless their P row sum passes 2^64 (then the max is raised, O rescaled in
-//    TMEM and the tile recomputed); P is rounded to bf16 and O is normalised
-//    by the row sum of that rounded P, while lse uses the unrounded sum.  At
-//    D = 64 a full 128-row tile's O leaves through the head slot's P buffer
-//    in shared memory and one TMA store; ragged last tiles use plain stores.
+//    in one pass, and S stays in TMEM until the tile's P row sum is checked:
+//    past 2^64 the tile is redone from TMEM with the max raised and O
+//    rescaled.  P is rounded to bf16 and O is normalised by the row sum of
+//    that rounded P, while lse uses the unrounded sum.  An item's epilogue
+//    runs during the head slot's next item's first tile; at D = 64 each
+//    warp's 32 full rows leave through a staging tile and one TMA store;
+//    ragged last tiles use plain stores.
 //
 // TMEM (512 columns): S0 S1 (128 each), O0 O1 (D each, plus at D = 64 the
-// 16 row-sum columns), and at D = 64 P0 P1 (keys 0..63, 32 columns each); at
+// 16 row-sum columns), and at D = 64 P0 P1 (keys 0..95, 48 columns each); at
 // D = 128 P aliases the first half of S.
 // Every wait is bounded; a timeout sets the device error word.
 #include <cuda.h>
@@ -52,6 +55,9 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kSumLimit = 18446744073709551616.0f;   // 2^64: tile row sum that forces a new max
+// D = 64: keys of P kept in TMEM (the rest of the tile's P goes through
+// shared memory); TMEM holds S, O with its row-sum columns and these.
+constexpr int kPTmemKeys = 96;
 // Every kPolyEvery-th pair of score columns takes its exponentials on the FMA
 // pipe (exp2_poly.cuh) instead of the MUFU; 0 = none.  The polynomial clamps
 // its argument to 2^126, which still trips the 2^64 row-sum check below.
@@ -81,11 +87,11 @@ struct PrefillCfg {
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kQBufs * 2 * kTile;
     static constexpr int kOffV = kOffK + kStagesK * kTile;
-    // At D = 64, P is split by keys: keys 0..63 go to TMEM (PV as TS MMA),
-    // keys 64..127 to shared memory (SS MMA), and the PV B operand is V
+    // At D = 64, P is split by keys: keys 0..95 go to TMEM (PV as TS MMA),
+    // keys 96..127 to shared memory (SS MMA), and the PV B operand is V
     // extended by a ones column, so the same MMA also accumulates the row sum
     // of the bf16-rounded P next to O (N = D + 16 costs no tensor time over
-    // N = D here).
+    // N = D here).  TMEM then holds exactly S, O and P of both head slots.
     static constexpr bool kSplitP = (D == 64);
     static constexpr int kON = kSplitP ? D + 16 : D;      // O accumulator columns
     static constexpr int kOffPb = kOffV + kStagesV * kTile;                 // per head 128 rows x 128 B
@@ -98,11 +104,11 @@ struct PrefillCfg {
     static constexpr int kSmem = 1024 + kOffBar + kNumBars * 8 + 16;
     static constexpr uint32_t kTmemCols = 512;
     // TMEM columns of head slot i (every region starts on a multiple of 32).
-    // D = 64:  S 0 | 128, O (+ row sum) 256 | 384, P keys 0..63 at 352 | 480.
+    // D = 64:  S 0 | 128, O (+ row sum) 256 | 384, P keys 0..95 at 336 | 464.
     // D = 128: S 0 | 128, O 256 | 384, P aliases the first half of S.
     static __device__ __forceinline__ uint32_t col_s(int i) { return i * 128; }
     static __device__ __forceinline__ uint32_t col_o(int i) { return 256 + i * 128; }
-    static __device__ __forceinline__ uint32_t col_p(int i) { return kSplitP ? 256 + i * 128 + 96 : i * 128; }
+    static __device__ __forceinline__ uint32_t col_p(int i) { return kSplitP ? 256 + i * 128 + kON : i * 128; }
 };
 
 struct PrefillArgs {
@@ -390,10 +396,11 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                     for (int kk = 0; kk < kPrefillKeys / 16; ++kk) {
                         const uint32_t vk = vb + kk * 2048;
                         const uint64_t bd = ptx::smem_desc_sw128(vk, ones - vk, 1024);
-                        if (kk < 4)
+                        if (kk < kPTmemKeys / 16)
                             ptx::tc_mma_ts(t_o, t_p + kk * 8, bd, idesc_pv, (!first || kk > 0) ? 1u : 0u);
                         else
-                            ptx::tc_mma_ss(t_o, ptx::smem_desc_sw128(pb + (kk - 4) * 32, 16, 1024), bd, idesc_pv, 1u);
+                            ptx::tc_mma_ss(t_o, ptx::smem_desc_sw128(pb + (kk - kPTmemKeys / 16) * 32, 16, 1024), bd,
+                                           idesc_pv, 1u);
                     }
                 } else {
 #pragma unroll
@@ -494,8 +501,9 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
         const uint32_t t_s = tmem + lane_off + C::col_s(i);
         const uint32_t t_o = tmem + lane_off + C::col_o(i);
         const uint32_t t_p = tmem + lane_off + C::col_p(i);
-        // This thread's row of P keys 64..127 in shared memory (D = 64): 128
-        // bytes, 16-byte chunks swizzled by the row (K-major SW128 A operand).
+        // This thread's row of P keys 96..127 in shared memory (D = 64): the
+        // first 64 bytes of a 128-byte row, 16-byte chunks swizzled by the
+        // row (K-major SW128 A operand).
         const uint32_t pb_row = sbase + C::kOffPb + i * C::kAtom + (r >> 3) * 1024 + (r & 7) * 128;
         const float sl2 = a.scale_log2;
         const float poly_a = sl2 * exp2poly::kInvRange;   // scale of the FMA-pipe pairs' argument
@@ -757,10 +765,15 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                 }
                 ptx::tmem_st32(t_p, pk[0]);
                 if constexpr (C::kSplitP) {
+                    // keys 64..95 to TMEM, 96..127 to shared memory
+                    uint32_t mid[16];
 #pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        ptx::st_shared_v4(pb_row + ((c ^ (r & 7)) << 4), pk[1][4 * c], pk[1][4 * c + 1],
-                                          pk[1][4 * c + 2], pk[1][4 * c + 3]);
+                    for (int e = 0; e < 16; ++e) mid[e] = pk[1][e];
+                    ptx::tmem_st16(t_p + 32, mid);
+#pragma unroll
+                    for (int c = 0; c < (kPrefillKeys - kPTmemKeys) / 8; ++c)
+                        ptx::st_shared_v4(pb_row + ((c ^ (r & 7)) << 4), pk[1][16 + 4 * c], pk[1][16 + 4 * c + 1],
+                                          pk[1][16 + 4 * c + 2], pk[1][16 + 4 * c + 3]);
                     ptx::fence_proxy_async_smem();   // the SS MMA reads it through the async proxy
                 } else {
                     ptx::tmem_st32(t_p + 32, pk[1]);
