@@ -448,10 +448,13 @@ def run_ours(args, world, rank, local):
         gmean = sum(gtimes) / len(gtimes) / 1e3
         if gplan.device_error():
             raise RuntimeError("graph decode recorded a device error")
-        graph = {"workload": "gptoss_decode, one CUDA-graph replay (device planner + persistent decode)",
+        # Plans for up to 128 requests are built inside the persistent decode
+        # grid (one kernel per replay); larger ones by a planner kernel first.
+        per_replay = 1 if batch.batch_size <= 128 else 2
+        graph = {"workload": "gptoss_decode, one CUDA-graph replay (device-built work list + persistent decode)",
                  "value": bytes_step / gmean / 1e9, "unit": "GB/s", "ms_per_step": gmean * 1e3,
                  "frac_of_hbm_peak": bytes_step / gmean / 1e9 / float(peaks["hbm_gbs"]),
-                 "steps": gsteps, "launches": 2 * gsteps, "clocks": gclocks}
+                 "steps": gsteps, "launches": per_replay * gsteps, "clocks": gclocks}
     except binding.AttnError as e:
         graph = {"unavailable": str(e)}
 
