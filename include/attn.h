@@ -272,9 +272,11 @@ ATTN_API attn_status attn_decode_noalloc_device_error(attn_plan_t plan, int32_t*
  * attn_graph_plan / attn_decode_graph -- decode that can be captured in a CUDA
  * graph and replayed for new batches.  The split-KV plan depends on the
  * requests' lengths, so host planning would freeze it at capture; here the
- * step's first kernel builds the work list on the device from device-resident
- * metadata, with the same rule as attn_plan, and a fixed grid of persistent
- * decode CTAs takes the units from a device queue ("Fast embeddings on GPUs"
+ * work list is built on the device from device-resident metadata, with the
+ * same rule as attn_plan (for plans of up to 128 requests by every CTA of the
+ * persistent decode grid itself, else by a planner kernel launched first),
+ * and a fixed grid of persistent decode CTAs takes the units from a device
+ * queue ("Fast embeddings on GPUs"
  * (Perplexity), section "Managing CUDA graphs": kernels that configure their
  * launches from dynamic host inputs prevent full CUDA graphs; the page's fix
  * is to change those kernels so they can be captured).
