@@ -168,6 +168,30 @@ def test_cuda_graph_capture_replays_new_batches():
         _check(b, buf, n=400, seed=k, what=f"replay {k}")
 
 
+@pytest.mark.parametrize("max_batch", [128, 200])
+def test_graph_empty_and_full_batches(max_batch):
+    """B = 0 leaves every row untouched and records no error; B = max_batch
+    fills the plan (128: the most the in-grid plan takes; 200: the planner
+    kernel).  Both paths, one plan, one after the other."""
+    kv = np.random.default_rng(17).integers(1, 1200, size=max_batch).tolist()
+    b = syn.make_batch("full", [1] * max_batch, kv, 16, 2, 64, 16, seed=17)
+    buf = Buffers(max_batch, 16, 2, 64, 16, b.num_pages, len(b.page_table))
+    buf.load(b)
+    plan = _graph_plan(buf, max_batch, b)
+    buf.batch.fill_(0)
+    _decode(plan, buf)
+    torch.cuda.synchronize()
+    assert plan.device_error() == 0
+    assert len(plan.device_units()) == 0
+    assert torch.isnan(buf.out.float()).all()
+    buf.batch.fill_(max_batch)
+    _decode(plan, buf)
+    torch.cuda.synchronize()
+    assert plan.device_error() == 0
+    _check(b, buf, n=500, seed=3, what=f"graph decode, {max_batch} of {max_batch} requests")
+    assert torch.isfinite(buf.out.float()).all()
+
+
 def test_graph_malformed_request_sets_plan_error():
     b = syn.make_batch("bad", [1, 1, 1], [40, 90, 7], 8, 2, 64, 16, seed=11)
     buf = Buffers(4, 8, 2, 64, 16, b.num_pages, len(b.page_table))
