@@ -306,10 +306,10 @@ decode_sink_attn_kernel(const __grid_constant__ CUtensorMap kv_map, const Decode
     const uint64_t policy = ptx::policy_evict_first();
     int gbase = 0;   // stage uses of this warp's ring so far (across units)
 
-    // The persistent grid is launched as a programmatic dependent of the
-    // device planner: its CTAs start (and do the set-up above) while the
-    // planner runs, and wait here until the planner's unit list is complete
-    // and visible.  Without such a launch the wait returns at once.
+    // Behind the planner kernel the persistent grid is launched as its
+    // programmatic dependent: its CTAs start (and do the set-up above) while
+    // the planner runs, and wait here until the planner's unit list is
+    // complete and visible.  Without such a launch the wait returns at once.
     if constexpr (kPersistent) asm volatile("griddepcontrol.wait;" ::: "memory");
     // In-grid plan: its tables sit past the decode's own shared memory.
     InPlan& ip = *reinterpret_cast<InPlan*>(smem + C::kSmem - 1024);

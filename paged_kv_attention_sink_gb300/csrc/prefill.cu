@@ -600,7 +600,7 @@ prefill_sink_attn_kernel(const __grid_constant__ CUtensorMap q_map,
         if (i == 1 && lane == 0) ptx::mbar_arrive(other_turn);
         // Item descriptors and sinks are read from L1: the sinks' lines are
         // prefetched here, each next descriptor after the current item's last
-        // tile (its latency then overlaps the wait for the last PV).
+        // tile.
         if (a.sinks != nullptr && lane * 32 < a.Hq) ptx::prefetch_l1(a.sinks + lane * 32);
         for (int item = item_begin; ok && item < item_end; ++item) {
             const PrefillItem it = a.items[item];
