@@ -31,6 +31,7 @@ rank time.  `--impl reference` times the CPU fp64 oracle instead.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import math
@@ -292,6 +293,42 @@ def run_reference(args, world, rank):
 
 
 # ---------------------------------------------------------------- our arm
+_cudart = None
+
+
+def cudart():
+    """The CUDA runtime libattn.so links, for the end-to-end loop's copies,
+    events and stream waits (ctypes signatures set once)."""
+    global _cudart
+    if _cudart is None:
+        import ctypes.util
+        rt = None
+        for name in ("libcudart.so.13", "libcudart.so.12", ctypes.util.find_library("cudart")):
+            if not name:
+                continue
+            try:
+                rt = ctypes.CDLL(name)
+                break
+            except OSError:
+                continue
+        if rt is None:
+            raise RuntimeError("the CUDA runtime library was not found")
+        vp, sz = ctypes.c_void_p, ctypes.c_size_t
+        for fn, args in (("cudaMemcpyAsync", [vp, vp, sz, ctypes.c_int, vp]), ("cudaEventRecord", [vp, vp]),
+                         ("cudaStreamWaitEvent", [vp, vp, ctypes.c_uint]), ("cudaEventSynchronize", [vp]),
+                         ("cudaEventCreateWithFlags", [ctypes.POINTER(vp), ctypes.c_uint]),
+                         ("cudaEventDestroy", [vp]), ("cudaGetLastError", [])):
+            f = getattr(rt, fn)
+            f.argtypes, f.restype = args, ctypes.c_int
+        _cudart = rt
+    return _cudart
+
+
+def rt_check(status, what):
+    if status != 0:
+        raise RuntimeError(f"{what}: CUDA error {status}")
+
+
 def traffic_for(kernel_file, key):
     """DRAM bytes per launch from a committed ncu summary, if the kernel source
     is unchanged since the capture (else None)."""
@@ -368,11 +405,11 @@ def run_ours(args, world, rank, local):
         sk = None if batch.sinks is None else torch.from_numpy(batch.sinks).to(dev)
         return q, kv, pt, sk
 
-    def plan_of(batch, pt, workspace=None):
+    def plan_of(batch, pt, workspace=None, stream=None):
         return binding.Plan(batch.qo_indptr, batch.kv_indptr, pt, batch.last_page_len,
                             batch.num_qo_heads, batch.num_kv_heads, batch.head_dim, batch.page_size,
                             causal=batch.causal, sm_scale=batch.sm_scale, num_pages=batch.num_pages,
-                            workspace=workspace)
+                            workspace=workspace, stream=stream)
 
     flush = L2Flush(dev)
     props = torch.cuda.get_device_properties(dev)
@@ -469,7 +506,12 @@ def run_ours(args, world, rank, local):
     # against the decode on the compute stream by events, so a step's copies
     # overlap its neighbours' decodes.
     # q and the page table share one pinned host buffer and one device buffer
-    # per slot (one upload); out and lse likewise (one read-back).
+    # per slot (one upload); out and lse likewise (one read-back).  The copies,
+    # events and stream waits go straight to the CUDA runtime the library
+    # links (ctypes), as a serving loop in C would make them: torch's stream
+    # switching and copy dispatch cost more host time per step than the
+    # planner itself, and with three steps in flight the host loop, not the
+    # GPU, then set the pace.
     q_bytes, pt_bytes = q.numel() * 2, pt.numel() * 4
     out_bytes, lse_bytes = out.numel() * 2, lse.numel() * 4
     in_h = torch.empty(q_bytes + pt_bytes, dtype=torch.uint8).pin_memory()
@@ -485,30 +527,37 @@ def run_ours(args, world, rank, local):
             "res": d_res, "out": d_res[:out_bytes].view(torch.bfloat16).view(out.shape),
             "lse": d_res[out_bytes:].view(torch.float32).view(lse.shape),
             "res_h": torch.empty(out_bytes + lse_bytes, dtype=torch.uint8).pin_memory(),
-            "ev": torch.cuda.Event(), "uploaded": torch.cuda.Event(), "decoded": torch.cuda.Event(),
             "plan": None, "ws": torch.empty(plan.info()["workspace_bytes"], dtype=torch.uint8, device=dev)})
     # A fixed 500 steps (about 50 ms), whatever --steps says: with three steps
     # in flight, a short region is dominated by filling and draining the
     # pipeline.
     e2e_steps = 500
     up_stream, down_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    rt = cudart()
+    s_up, s_down, s_main = (ctypes.c_void_p(x.cuda_stream) for x in (up_stream, down_stream, stream))
+    for sl in e2e_slots:
+        for name in ("ev", "uploaded", "decoded"):
+            ev = ctypes.c_void_p()
+            rt_check(rt.cudaEventCreateWithFlags(ctypes.byref(ev), 2), "cudaEventCreateWithFlags")   # no timing
+            sl[name] = ev
+        sl["in_p"], sl["res_p"] = ctypes.c_void_p(sl["in"].data_ptr()), ctypes.c_void_p(sl["res"].data_ptr())
+        sl["res_h_p"] = ctypes.c_void_p(sl["res_h"].data_ptr())
+    in_h_p, n_in, n_res = ctypes.c_void_p(in_h.data_ptr()), in_h.numel(), e2e_slots[0]["res_h"].numel()
     torch.cuda.synchronize()   # the slots' buffers exist before other streams touch them
 
     def e2e_step(k):
         sl = e2e_slots[k % 3]
         if sl["plan"] is not None:
-            sl["ev"].synchronize()   # step k-3's result is on the host; its buffers are free
-        with torch.cuda.stream(up_stream):
-            sl["in"].copy_(in_h, non_blocking=True)
-            sl["plan"] = plan_of(batch, sl["pt"], sl["ws"])   # binds: the work list goes up on up_stream
-            sl["uploaded"].record(up_stream)
-        stream.wait_event(sl["uploaded"])
+            rt.cudaEventSynchronize(sl["ev"])   # step k-3's result is on the host; its buffers are free
+        rt.cudaMemcpyAsync(sl["in_p"], in_h_p, n_in, 1, s_up)              # host to device
+        sl["plan"] = plan_of(batch, sl["pt"], sl["ws"], stream=up_stream)  # binds: the work list goes up on up_stream
+        rt.cudaEventRecord(sl["uploaded"], s_up)
+        rt.cudaStreamWaitEvent(s_main, sl["uploaded"], 0)
         sl["plan"].decode(sl["q"], kv, sinks, sl["out"], sl["lse"], stream=stream)
-        sl["decoded"].record(stream)
-        down_stream.wait_event(sl["decoded"])
-        with torch.cuda.stream(down_stream):
-            sl["res_h"].copy_(sl["res"], non_blocking=True)
-        sl["ev"].record(down_stream)
+        rt.cudaEventRecord(sl["decoded"], s_main)
+        rt.cudaStreamWaitEvent(s_down, sl["decoded"], 0)
+        rt.cudaMemcpyAsync(sl["res_h_p"], sl["res_p"], n_res, 2, s_down)  # device to host
+        rt.cudaEventRecord(sl["ev"], s_down)
 
     for k in range(3):
         e2e_step(k)
@@ -519,6 +568,10 @@ def run_ours(args, world, rank, local):
         e2e_step(k)
     torch.cuda.synchronize()
     e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    rt_check(rt.cudaGetLastError(), "e2e loop")
+    for sl in e2e_slots:
+        for name in ("ev", "uploaded", "decoded"):
+            rt.cudaEventDestroy(sl[name])
     if not torch.equal(e2e_slots[0]["res_h"], e2e_slots[1]["res_h"]):
         raise RuntimeError("end-to-end decode steps on the same batch disagree")
     units = plan.info()["num_decode_units"]
